@@ -1,0 +1,407 @@
+"""Benchmark of the chunked causal 3-D convolution on GB300.
+
+One step = one pass of the whole hot path over one decoder layer's worth of
+frames: the chunk loop (chunks of 4 frames, the 2-frame temporal cache carried
+from chunk to chunk in two ping-pong buffers), each chunk one launch of the
+tensor-core kernel (implicit-GEMM conv + bias + residual epilogue + cache
+update).  Inputs are resident in HBM before the timed region and larger than
+L2.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (host cores), printing the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal conv3d TFLOP/s"
+UNIT = "TFLOP/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tc_bf16_kernel_traffic.json")
+KERNEL_SOURCE = os.path.join(ROOT, "chunked_causal_convolution_gb300", "csrc", "cc3d_tc.cu")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_per_launch(workload):
+    """DRAM bytes per launch from the committed ncu capture, if it was taken on this kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        if t.get("kernel_source_sha") == kernel_source_sha() and t.get("workload") == workload:
+            return float(t["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload_config(wl):
+    return {
+        "workload": "%s: causal conv3d Cin=%d Cout=%d k=3x3x3, T=%d frames in chunks %s with a 2-frame "
+                    "cache, H=%d W=%d, batch 1, bias%s" % (
+                        wl.name, wl.Cin, wl.Cout, wl.T, "x".join(str(c) for c in sorted(set(wl.chunks))),
+                        wl.H, wl.W, " + residual" if wl.r is not None else ""),
+        "Cin": wl.Cin, "Cout": wl.Cout, "T": wl.T, "H": wl.H, "W": wl.W, "chunks": list(wl.chunks),
+        "flop_per_step": wl.flops,
+        "l2": "inputs larger than L2 (%.2f GB per activation tensor vs 129 MB L2), no flush" % (
+            wl.T * wl.H * wl.W * wl.Cin * 2 / 1e9),
+    }
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample(wl, rows, nthreads=None):
+    """Time the oracle's chunk form on one output frame (first `rows` rows) of the workload, from its
+    2-frame history: returns (metric FLOPs of the outputs computed, seconds, threads)."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    import synth
+    from synth import native
+
+    t0 = wl.T // 2
+    H, W, C = rows, wl.W, wl.Cin
+
+    def gen(tid, dist, shape, frame0):
+        # rows 0..rows-1 of frames frame0.. of the global video
+        f, h = np.meshgrid(np.arange(shape[0]), np.arange(shape[1]), indexing="ij")
+        base = ((frame0 + f) * wl.H + h) * wl.W * shape[3]
+        e = base[..., None, None] + (np.arange(shape[2])[:, None] * shape[3] + np.arange(shape[3]))[None, None]
+        parts = np.array_split(e.reshape(-1), 16)
+        with ThreadPoolExecutor(16) as ex:
+            vals = list(ex.map(lambda p: native.values_host(wl.seed, tid, dist, p, wl.dtype), parts))
+        raw = np.concatenate(vals).reshape(shape)
+        return synth.bf16_bits_to_f64(raw) if wl.dtype == "bf16" else raw.astype(np.float64)
+
+    hist = gen(synth.TID_X, wl.x, (2, H, W, C), t0 - 2)
+    x = gen(synth.TID_X, wl.x, (1, H, W, C), t0)
+    w = synth.bf16_bits_to_f64(native.values_host(wl.seed, synth.TID_W, wl.w,
+                                                  synth.dense_index((wl.Cout, 3, 3, 3, C)), wl.dtype))
+    b = synth.bf16_bits_to_f64(native.values_host(wl.seed, synth.TID_B, wl.b, np.arange(wl.Cout), wl.dtype))
+    r = gen(synth.TID_R, wl.r, (1, H, W, wl.Cout), t0) if wl.r is not None else None
+    n = nthreads or oracle.default_threads()
+    ts = time.perf_counter()
+    oracle.conv_chunk(x, w, b, r, hist, nthreads=n)
+    dt = time.perf_counter() - ts
+    flops = 2.0 * wl.Cin * wl.Cout * 27 * H * W
+    return flops, dt, n
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(wl, rows)
+    times, flops, n = [], 0.0, 1
+    for _ in range(args.steps):
+        flops, dt, n = oracle_sample(wl, rows)
+        times.append(dt)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    sample = ("fp64 oracle chunk form: %d of %d rows of one output frame (frame %d) of %s from its 2-frame "
+              "history, per step" % (rows, wl.H, wl.T // 2, wl.name))
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args, wl):
+    import torch
+
+    import chunked_causal_convolution_gb300 as cc3d
+    import synth
+    from synth import native
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+    __graft_entry__.build()
+
+    dev = torch.device("cuda", local)
+    dt = torch.bfloat16
+    T, H, W = wl.T, wl.H, wl.W
+    x = native.fill_device(torch.empty((T, H, W, wl.Cin), dtype=dt, device=dev), wl.seed, synth.TID_X, wl.x)
+    wt = native.fill_device(torch.empty((wl.Cout, 3, 3, 3, wl.Cin), dtype=dt, device=dev), wl.seed,
+                            synth.TID_W, wl.w)
+    b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device=dev), wl.seed, synth.TID_B, wl.b)
+    r = None
+    if wl.r is not None:
+        r = native.fill_device(torch.empty((T, H, W, wl.Cout), dtype=dt, device=dev), wl.seed, synth.TID_R, wl.r)
+    y = torch.empty((T, H, W, wl.Cout), dtype=dt, device=dev)
+    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, H, W, dtype="bf16")
+    caches = [plan.new_cache(dev), plan.new_cache(dev)]
+    stream = torch.cuda.Stream(device=dev)
+    bounds = []
+    s = 0
+    for c in wl.chunks:
+        bounds.append((s, c))
+        s += c
+
+    def step(ev_pairs=None, xs=x, rs=r, ys=y):
+        for k, (s0, c) in enumerate(bounds):
+            if ev_pairs is not None:
+                ev_pairs[k][0].record(stream)
+            cc3d.cc3d_forward_chunk(plan.handle, c, xs[s0:s0 + c], wt, b,
+                                    rs[s0:s0 + c] if rs is not None else None,
+                                    caches[k % 2] if k else None, caches[(k + 1) % 2], ys[s0:s0 + c], stream)
+            if ev_pairs is not None:
+                ev_pairs[k][1].record(stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    if plan.status(stream) != 0:
+        raise RuntimeError("device status after warm-up: %s" % cc3d.cc3d_status_string(plan.status(stream)))
+
+    # ---- timed region: K steps, events on the launching stream
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launch_evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in bounds] for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.25)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                step(launch_evs[i])
+            end.record(stream)
+        stream.synchronize()
+        time.sleep(0.25)
+    barrier()
+    ms = start.elapsed_time(end)
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    st = plan.status(stream)
+    if st != 0:
+        raise RuntimeError("device status after timing: %s" % cc3d.cc3d_status_string(st))
+    ms_per_step = ms / args.steps
+    value = wl.flops * world * args.steps / (ms / 1e3) / 1e12
+    # per-launch durations of the dominant (only) kernel
+    launch_ms = [a.elapsed_time(bb) for row in launch_evs for (a, bb) in row]
+    full = [ms_ for ms_, (_, c) in zip(launch_ms, bounds * args.steps) if c == max(wl.chunks)]
+    avg_launch_ms = sum(full) / len(full)
+    flop_per_launch = wl.flops / T * max(wl.chunks)
+    p, src = peaks()
+    achieved = flop_per_launch / (avg_launch_ms / 1e3) / 1e12
+    peak = float(p["bf16_tflops"])
+    traffic = traffic_per_launch(wl.name)
+
+    # ---- end to end: pinned host inputs -> device -> chunk loop -> host result, every step
+    xh = x.cpu().pin_memory()
+    rh = r.cpu().pin_memory() if r is not None else None
+    yh = torch.empty(y.shape, dtype=dt).pin_memory()
+    xd, rd, yd = torch.empty_like(x), (torch.empty_like(r) if r is not None else None), torch.empty_like(y)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            xd.copy_(xh, non_blocking=True)
+            if rh is not None:
+                rd.copy_(rh, non_blocking=True)
+            step(xs=xd, rs=rd, ys=yd)
+            yh.copy_(yd, non_blocking=True)
+    stream.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            xd.copy_(xh, non_blocking=True)
+            if rh is not None:
+                rd.copy_(rh, non_blocking=True)
+            step(xs=xd, rs=rd, ys=yd)
+            yh.copy_(yd, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    if not torch.equal(yh.to(dev), y):
+        raise RuntimeError("end-to-end result differs from the device-resident result")
+    h2d = x.numel() * 2 + (r.numel() * 2 if r is not None else 0)
+    d2h = y.numel() * 2
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        flops, secs, n = oracle_sample(wl, args.ref_rows)
+        cpu = {"value": flops / secs / 1e12, "unit": UNIT, "cores": n, "kind": "oracle",
+               "sample": "fp64 oracle chunk form: %d of %d rows of one output frame (frame %d) of %s from its "
+                         "2-frame history (%.1f s)" % (args.ref_rows, wl.H, wl.T // 2, wl.name, secs)}
+
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    peak_note = "%s MEASURED_PEAKS bf16_tflops (burst, kernel timed alone)" % src
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator, on device)",
+        "config": workload_config(wl),
+        "output_frames_per_s": wl.T * world * args.steps / (ms / 1e3),
+        "pct_of_dense_bf16_peak": {"measured_burst": 100 * value / world / float(p["bf16_tflops"]),
+                                   "measured_sustained": 100 * value / world / float(p["bf16_tflops_sustained"]),
+                                   "spec_2250": 100 * value / world / 2250.0},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
+                     "kernel": "tc_bf16_kernel", "flop_per_launch": flop_per_launch,
+                     "avg_launch_ms": avg_launch_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": wl.flops * world * args.steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": args.steps * len(bounds) * plan.launches_per_chunk,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c96_residual")
+    ap.add_argument("--ref-rows", type=int, default=90, help="rows of the oracle sample frame")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("warm-up raised to 3 steps")
+        args.warmup = 3
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    if wl.T * wl.H * wl.W * max(wl.Cin, wl.Cout) * 2 > 32e9:
+        log("%s does not fit resident on one device; it is covered by the streaming parity test" % wl.name)
+        return 2
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

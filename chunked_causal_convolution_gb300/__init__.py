@@ -1,0 +1,258 @@
+"""Chunked causal 3-D convolution for GB300 (sm_103a): Python binding of libcc3d.so.
+
+This module only marshals arguments: every step of the convolution (the
+implicit-GEMM tensor-core kernel, its fused bias / residual epilogue, the
+temporal-cache update, the float32 CUDA-core kernel) runs in the CUDA kernels
+of ``libcc3d.so``.  PyTorch is used for device memory and streams only.  There
+is no CPU or library fallback: if the shared library is missing, every call
+raises.
+
+The functions carry the C ABI's names (``include/cc3d.h``):
+
+    plan = cc3d_plan_create(Cin, Cout, H, W, kt, kh, kw, dtype)
+    cc3d_forward_chunk(plan, T, x, w, b, residual, cache_in, cache_out, y, stream)
+    cc3d_reset(plan, cache, stream); cc3d_get_status(plan, stream); cc3d_destroy(plan)
+
+where tensor arguments are CUDA tensors (or raw device addresses as ints, or
+None) and ``stream`` is a ``torch.cuda.Stream``, a raw handle or None (the
+current stream).  :class:`CausalConv3dPlan` wraps the same calls.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "CC3D_F32", "CC3D_BF16", "CC3DError", "CausalConv3dPlan",
+    "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_reset", "cc3d_get_status", "cc3d_destroy",
+    "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
+    "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "library_path", "load_library",
+    "weights_from_torch_layout", "EXPORTED_SYMBOLS",
+]
+
+CC3D_F32 = 0
+CC3D_BF16 = 1
+
+STATUS_NAMES = {
+    0: "CC3D_OK", 1: "CC3D_ERR_INVALID_ARG", 2: "CC3D_ERR_UNSUPPORTED", 3: "CC3D_ERR_ALIGNMENT",
+    4: "CC3D_ERR_ALIAS", 5: "CC3D_ERR_CUDA", 6: "CC3D_ERR_OOM", 7: "CC3D_ERR_DEVICE_TIMEOUT",
+    8: "CC3D_ERR_NOT_DEVICE_MEMORY",
+}
+
+EXPORTED_SYMBOLS = (
+    "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_reset", "cc3d_get_status", "cc3d_destroy",
+    "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
+    "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault",
+)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+_lock = threading.Lock()
+
+
+class CC3DError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        self.name = STATUS_NAMES.get(code, str(code))
+        msg = "%s (%s)" % (self.name, _status_text(code))
+        super().__init__("%s: %s" % (what, msg) if what else msg)
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libcc3d.so")
+
+
+def load_library():
+    """Load libcc3d.so (built in-tree by ``build.py``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError("libcc3d.so is not built (expected at %s); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+        lib = ctypes.CDLL(path)
+        vp, i, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong
+        lib.cc3d_plan_create.argtypes = [i] * 8 + [ctypes.POINTER(vp)]
+        lib.cc3d_forward_chunk.argtypes = [vp, i] + [vp] * 8
+        lib.cc3d_reset.argtypes = [vp, vp, vp]
+        lib.cc3d_get_status.argtypes = [vp, vp]
+        lib.cc3d_destroy.argtypes = [vp]
+        lib.cc3d_destroy.restype = None
+        lib.cc3d_status_string.argtypes = [i]
+        lib.cc3d_status_string.restype = ctypes.c_char_p
+        lib.cc3d_plan_kernel.argtypes = [vp]
+        lib.cc3d_plan_kernel.restype = ctypes.c_char_p
+        lib.cc3d_plan_launches_per_chunk.argtypes = [vp]
+        lib.cc3d_debug_set_wait_budget_ns.argtypes = [vp, u64]
+        lib.cc3d_debug_set_fault.argtypes = [vp, i]
+        for f in (lib.cc3d_plan_create, lib.cc3d_forward_chunk, lib.cc3d_reset, lib.cc3d_get_status,
+                  lib.cc3d_plan_launches_per_chunk, lib.cc3d_debug_set_wait_budget_ns,
+                  lib.cc3d_debug_set_fault):
+            f.restype = i
+        _lib = lib
+        return lib
+
+
+def _status_text(code: int) -> str:
+    try:
+        return load_library().cc3d_status_string(code).decode()
+    except Exception:
+        return STATUS_NAMES.get(code, "?")
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise CC3DError(code, what)
+
+
+def _dtype_code(dtype) -> int:
+    if dtype in (CC3D_F32, CC3D_BF16):
+        return dtype
+    s = str(dtype)
+    if s in ("bf16", "bfloat16", "torch.bfloat16"):
+        return CC3D_BF16
+    if s in ("f32", "float32", "torch.float32"):
+        return CC3D_F32
+    raise ValueError("unsupported dtype %r" % (dtype,))
+
+
+def _addr(t):
+    """Device address of a tensor argument (tensor, int address or None)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t or None
+    if not t.is_cuda:
+        raise ValueError("tensor arguments must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous")
+    return t.data_ptr() or None
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+# ---------------------------------------------------------------- C-ABI names
+def cc3d_plan_create(Cin, Cout, H, W, kt=3, kh=3, kw=3, dtype=CC3D_BF16):
+    h = ctypes.c_void_p()
+    _check(load_library().cc3d_plan_create(int(Cin), int(Cout), int(H), int(W), int(kt), int(kh), int(kw),
+                                           _dtype_code(dtype), ctypes.byref(h)), "cc3d_plan_create")
+    return h.value
+
+
+def cc3d_forward_chunk(plan, T, x, w, b, residual, cache_in, cache_out, y, stream=None):
+    _check(load_library().cc3d_forward_chunk(plan, int(T), _addr(x), _addr(w), _addr(b), _addr(residual),
+                                             _addr(cache_in), _addr(cache_out), _addr(y), _stream(stream)),
+           "cc3d_forward_chunk")
+
+
+def cc3d_reset(plan, cache, stream=None):
+    _check(load_library().cc3d_reset(plan, _addr(cache), _stream(stream)), "cc3d_reset")
+
+
+def cc3d_get_status(plan, stream=None) -> int:
+    """Synchronise the stream and return the status code (0 = ok); never raises on device errors."""
+    return int(load_library().cc3d_get_status(plan, _stream(stream)))
+
+
+def cc3d_destroy(plan):
+    if plan:
+        load_library().cc3d_destroy(plan)
+
+
+def cc3d_status_string(code: int) -> str:
+    return load_library().cc3d_status_string(int(code)).decode()
+
+
+def cc3d_plan_kernel(plan) -> str:
+    s = load_library().cc3d_plan_kernel(plan)
+    return s.decode() if s else ""
+
+
+def cc3d_plan_launches_per_chunk(plan) -> int:
+    return int(load_library().cc3d_plan_launches_per_chunk(plan))
+
+
+def cc3d_debug_set_wait_budget_ns(plan, ns: int):
+    _check(load_library().cc3d_debug_set_wait_budget_ns(plan, int(ns)), "cc3d_debug_set_wait_budget_ns")
+
+
+def cc3d_debug_set_fault(plan, mode: int):
+    _check(load_library().cc3d_debug_set_fault(plan, int(mode)), "cc3d_debug_set_fault")
+
+
+# ---------------------------------------------------------------- convenience
+def weights_from_torch_layout(w_oikkk):
+    """PyTorch Conv3d weights [Cout][Cin][kt][kh][kw] -> this library's [Cout][kt][kh][kw][Cin]."""
+    return w_oikkk.permute(0, 2, 3, 4, 1).contiguous()
+
+
+class CausalConv3dPlan:
+    """One layer shape; owns the C plan.  Tensors are NDHWC (batch 1) CUDA tensors."""
+
+    def __init__(self, Cin, Cout, H, W, kt=3, kh=3, kw=3, dtype="bf16"):
+        self.Cin, self.Cout, self.H, self.W = int(Cin), int(Cout), int(H), int(W)
+        self.kt, self.kh, self.kw = int(kt), int(kh), int(kw)
+        self.dtype = _dtype_code(dtype)
+        self.handle = cc3d_plan_create(Cin, Cout, H, W, kt, kh, kw, self.dtype)
+
+    @property
+    def kernel(self) -> str:
+        return cc3d_plan_kernel(self.handle)
+
+    @property
+    def launches_per_chunk(self) -> int:
+        return cc3d_plan_launches_per_chunk(self.handle)
+
+    def torch_dtype(self):
+        import torch
+        return torch.float32 if self.dtype == CC3D_F32 else torch.bfloat16
+
+    def new_cache(self, device="cuda"):
+        """A zeroed history buffer [kt-1][H][W][Cin] (allocated by PyTorch, zeroed by the library)."""
+        import torch
+        c = torch.empty((self.kt - 1, self.H, self.W, self.Cin), dtype=self.torch_dtype(), device=device)
+        if self.kt > 1:
+            self.reset(c)
+        return c
+
+    def forward_chunk(self, x, w, b=None, residual=None, cache_in=None, cache_out=None, y=None, stream=None):
+        """Enqueue one chunk; returns y ([T][H][W][Cout]).  cache_out receives the new history."""
+        import torch
+        T = 0 if x is None else int(x.shape[0])
+        if y is None and T > 0:
+            y = torch.empty((T, self.H, self.W, self.Cout), dtype=self.torch_dtype(), device=x.device)
+        cc3d_forward_chunk(self.handle, T, x, w, b, residual, cache_in, cache_out, y, stream)
+        return y
+
+    def reset(self, cache, stream=None):
+        cc3d_reset(self.handle, cache, stream)
+
+    def status(self, stream=None) -> int:
+        return cc3d_get_status(self.handle, stream)
+
+    def set_wait_budget_ns(self, ns):
+        cc3d_debug_set_wait_budget_ns(self.handle, ns)
+
+    def set_fault(self, mode):
+        cc3d_debug_set_fault(self.handle, mode)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            cc3d_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,351 @@
+// cc3d_api.cu -- the C ABI declared in include/cc3d.h: plans, argument checks, tensor-map
+// encoding and kernel dispatch.  Nothing here computes on the host; every step of the
+// convolution runs in the kernels of cc3d_tc.cu / cc3d_simt.cu.
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/cc3d.h"
+#include "cc3d_internal.h"
+
+namespace cc3d {
+
+// Per-device status word: kernels or-in STATUS_* bits, cc3d_get_status reads and clears it.
+__device__ unsigned g_status_word;
+
+namespace {
+
+enum KernelKind { K_SIMT_F32 = 0, K_TC_BF16 = 1, K_TC_BF16_NARROW = 2 };
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool sm103 = false;
+    int sms = 0;
+    unsigned* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cc3d_status device_info(DeviceInfo** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CC3D_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return CC3D_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return CC3D_ERR_CUDA;
+        if (g_encode == nullptr) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                fn == nullptr)
+                return CC3D_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.sm103 = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.status = static_cast<unsigned*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return CC3D_OK;
+}
+
+bool is_device_ptr(const void* p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the non-sticky error
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+}  // namespace cc3d
+
+using namespace cc3d;
+
+struct cc3d_plan_s {
+    int Cin, Cout, H, W, kt, kh, kw;
+    cc3d_dtype dtype;
+    int kind;
+    int CB;
+    unsigned long long wait_ns;
+    int fault;
+};
+
+extern "C" {
+
+const char* cc3d_status_string(cc3d_status s)
+{
+    switch (s) {
+    case CC3D_OK: return "ok";
+    case CC3D_ERR_INVALID_ARG: return "invalid argument";
+    case CC3D_ERR_UNSUPPORTED: return "unsupported shape, dtype or device";
+    case CC3D_ERR_ALIGNMENT: return "pointer not aligned (16 bytes for bf16, 4 for fp32)";
+    case CC3D_ERR_ALIAS: return "output buffer overlaps another buffer";
+    case CC3D_ERR_CUDA: return "CUDA runtime error";
+    case CC3D_ERR_OOM: return "out of host memory";
+    case CC3D_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case CC3D_ERR_NOT_DEVICE_MEMORY: return "pointer is not device memory";
+    }
+    return "unknown status";
+}
+
+cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, int kw, cc3d_dtype dtype,
+                             cc3d_plan_t* out)
+{
+    if (out == nullptr) return CC3D_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (Cin < 1 || Cout < 1 || H < 1 || W < 1 || kt < 1 || kh < 1 || kw < 1) return CC3D_ERR_INVALID_ARG;
+    if (kh % 2 == 0 || kw % 2 == 0) return CC3D_ERR_INVALID_ARG;
+    if (dtype != CC3D_F32 && dtype != CC3D_BF16) return CC3D_ERR_INVALID_ARG;
+    if ((long long)H * W > (1LL << 30) || Cin > 65536 || Cout > 65536) return CC3D_ERR_UNSUPPORTED;
+    int kind, CB = 0;
+    if (dtype == CC3D_F32) {
+        if (kt > 4 || kh > 5 || kw > 5) return CC3D_ERR_UNSUPPORTED;
+        kind = K_SIMT_F32;
+    } else {
+        if (kt != 3 || kh != 3 || kw != 3) return CC3D_ERR_UNSUPPORTED;
+        if (Cin % 16 != 0 || Cin > 1024) return CC3D_ERR_UNSUPPORTED;
+        if (!(Cout < 16 || (Cout % 16 == 0 && Cout <= 512))) return CC3D_ERR_UNSUPPORTED;
+        CB = (Cin % 32 == 0) ? 32 : 16;
+        TcLaunch probe;
+        memset(&probe, 0, sizeof(probe));
+        if (!tc_configure(CB, 1, H, W, Cin, Cout, &probe)) return CC3D_ERR_UNSUPPORTED;
+        kind = Cout < 16 ? K_TC_BF16_NARROW : K_TC_BF16;
+    }
+    cc3d_plan_s* p = new (std::nothrow) cc3d_plan_s;
+    if (p == nullptr) return CC3D_ERR_OOM;
+    p->Cin = Cin;
+    p->Cout = Cout;
+    p->H = H;
+    p->W = W;
+    p->kt = kt;
+    p->kh = kh;
+    p->kw = kw;
+    p->dtype = dtype;
+    p->kind = kind;
+    p->CB = CB;
+    p->wait_ns = 2000000000ull;
+    p->fault = 0;
+    *out = p;
+    return CC3D_OK;
+}
+
+void cc3d_destroy(cc3d_plan_t plan) { delete plan; }
+
+const char* cc3d_plan_kernel(cc3d_plan_t plan)
+{
+    if (plan == nullptr) return nullptr;
+    switch (plan->kind) {
+    case K_SIMT_F32: return "simt_f32";
+    case K_TC_BF16: return "tc_bf16";
+    default: return "tc_bf16_narrow";
+    }
+}
+
+int cc3d_plan_launches_per_chunk(cc3d_plan_t plan)
+{
+    if (plan == nullptr) return 0;
+    return plan->kind == K_SIMT_F32 ? 2 : 1;  // the tensor-core kernel also writes the new cache
+}
+
+cc3d_status cc3d_debug_set_wait_budget_ns(cc3d_plan_t plan, unsigned long long ns)
+{
+    if (plan == nullptr || ns == 0) return CC3D_ERR_INVALID_ARG;
+    plan->wait_ns = ns;
+    return CC3D_OK;
+}
+
+cc3d_status cc3d_debug_set_fault(cc3d_plan_t plan, int mode)
+{
+    if (plan == nullptr || mode < 0 || mode > 2) return CC3D_ERR_INVALID_ARG;
+    plan->fault = mode;
+    return CC3D_OK;
+}
+
+static size_t esize(const cc3d_plan_s* p) { return p->dtype == CC3D_F32 ? 4 : 2; }
+
+cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream)
+{
+    if (plan == nullptr || cache == nullptr) return CC3D_ERR_INVALID_ARG;
+    if (!aligned_to(cache, plan->dtype == CC3D_F32 ? 4 : 16)) return CC3D_ERR_ALIGNMENT;
+    if (!is_device_ptr(cache)) return CC3D_ERR_NOT_DEVICE_MEMORY;
+    const size_t bytes = (size_t)(plan->kt - 1) * plan->H * plan->W * plan->Cin * esize(plan);
+    if (bytes == 0) return CC3D_OK;
+    DeviceInfo* d = nullptr;
+    cc3d_status st = device_info(&d);
+    if (st != CC3D_OK) return st;
+    if (!d->sm103) return CC3D_ERR_UNSUPPORTED;
+    return zero_fill_launch(cache, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CC3D_OK
+                                                                                            : CC3D_ERR_CUDA;
+}
+
+cc3d_status cc3d_get_status(cc3d_plan_t plan, void* stream)
+{
+    if (plan == nullptr) return CC3D_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    cc3d_status st = device_info(&d);
+    if (st != CC3D_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CC3D_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return CC3D_ERR_CUDA;
+    if (word != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return CC3D_ERR_CUDA;
+        return CC3D_ERR_DEVICE_TIMEOUT;
+    }
+    return CC3D_OK;
+}
+
+cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b,
+                               const void* res, const void* cache_in, void* cache_out, void* y, void* stream_)
+{
+    if (plan == nullptr || T < 0) return CC3D_ERR_INVALID_ARG;
+    const cc3d_plan_s& p = *plan;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const size_t es = esize(&p);
+    const int P = p.kt - 1;
+    const size_t frame_in = (size_t)p.H * p.W * p.Cin * es;
+    const size_t frame_out = (size_t)p.H * p.W * p.Cout * es;
+    const size_t n_x = (size_t)T * frame_in, n_y = (size_t)T * frame_out;
+    const size_t n_cache = (size_t)P * frame_in;
+    const size_t n_w = (size_t)p.Cout * p.kt * p.kh * p.kw * p.Cin * es, n_b = (size_t)p.Cout * es;
+
+    // ---- presence
+    if (P > 0 && cache_out == nullptr) return CC3D_ERR_INVALID_ARG;
+    if (T > 0 && (x == nullptr || w == nullptr || y == nullptr)) return CC3D_ERR_INVALID_ARG;
+    if ((long long)T * p.H * p.W > (1LL << 40)) return CC3D_ERR_UNSUPPORTED;
+    // ---- alignment: 16 bytes for the tensor-core path (TMA), one element for fp32
+    const uintptr_t align = p.dtype == CC3D_F32 ? 4 : 16;
+    const void* all[] = {x, w, b, res, cache_in, cache_out, y};
+    for (const void* q : all)
+        if (q != nullptr && !aligned_to(q, align)) return CC3D_ERR_ALIGNMENT;
+    // ---- overlaps: outputs against everything else
+    struct Span {
+        const void* p;
+        size_t n;
+    };
+    const Span ins[] = {{T > 0 ? x : nullptr, n_x}, {T > 0 ? w : nullptr, n_w}, {T > 0 ? b : nullptr, n_b},
+                        {T > 0 ? res : nullptr, n_y}, {cache_in, n_cache}};
+    for (const Span& s : ins) {
+        if (T > 0 && overlaps(y, n_y, s.p, s.n)) return CC3D_ERR_ALIAS;
+        if (P > 0 && overlaps(cache_out, n_cache, s.p, s.n)) return CC3D_ERR_ALIAS;
+    }
+    if (T > 0 && P > 0 && overlaps(y, n_y, cache_out, n_cache)) return CC3D_ERR_ALIAS;
+    // ---- device memory
+    for (const void* q : all)
+        if (q != nullptr && !is_device_ptr(q)) return CC3D_ERR_NOT_DEVICE_MEMORY;
+    DeviceInfo* d = nullptr;
+    cc3d_status st = device_info(&d);
+    if (st != CC3D_OK) return st;
+    if (!d->sm103) return CC3D_ERR_UNSUPPORTED;
+
+    if (T == 0) {
+        // only the history moves: cache_out = last P frames of cache_in (or zeros)
+        if (P == 0) return CC3D_OK;
+        return cache_update_launch(nullptr, cache_in, cache_out, 0, P, frame_in, stream) == cudaSuccess
+                   ? CC3D_OK
+                   : CC3D_ERR_CUDA;
+    }
+
+    if (p.kind == K_SIMT_F32) {
+        SimtLaunch L;
+        L.T = T;
+        L.H = p.H;
+        L.W = p.W;
+        L.Cin = p.Cin;
+        L.Cout = p.Cout;
+        L.kt = p.kt;
+        L.kh = p.kh;
+        L.kw = p.kw;
+        L.x = static_cast<const float*>(x);
+        L.cache_in = static_cast<const float*>(cache_in);
+        L.w = static_cast<const float*>(w);
+        L.bias = static_cast<const float*>(b);
+        L.res = static_cast<const float*>(res);
+        L.y = static_cast<float*>(y);
+        if (simt_f32_launch(L, stream) != cudaSuccess) return CC3D_ERR_CUDA;
+        if (P > 0 && cache_update_launch(x, cache_in, cache_out, T, P, frame_in, stream) != cudaSuccess)
+            return CC3D_ERR_CUDA;
+        return CC3D_OK;
+    }
+
+    // ---- tensor-core path
+    TcLaunch L;
+    memset(&L, 0, sizeof(L));
+    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, &L)) return CC3D_ERR_UNSUPPORTED;
+    if (p.fault == 2) return CC3D_ERR_CUDA;  // injected host-side encode failure: nothing launched
+    const CUtensorMapSwizzle sw = p.CB == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : p.CB == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)T};
+        const cuuint64_t strides[3] = {(cuuint64_t)p.Cin * 2, (cuuint64_t)p.W * p.Cin * 2,
+                                       (cuuint64_t)p.H * p.W * p.Cin * 2};
+        const cuuint32_t box[4] = {(cuuint32_t)p.CB, (cuuint32_t)L.g.Sp, (cuuint32_t)L.g.nrows, 1};
+        if (g_encode(&L.map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CC3D_ERR_CUDA;
+        if (cache_in != nullptr) {
+            const cuuint64_t cdims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)P};
+            if (g_encode(&L.map_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache_in), cdims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return CC3D_ERR_CUDA;
+        }
+    }
+    {
+        // weights [Cout][27][Cin] seen as (ci, co, tap) so one box holds `taps_b` K-major tap tiles
+        const cuuint64_t dims[3] = {(cuuint64_t)p.Cin, (cuuint64_t)p.Cout, 27};
+        const cuuint64_t strides[2] = {(cuuint64_t)27 * p.Cin * 2, (cuuint64_t)p.Cin * 2};
+        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)L.NT, (cuuint32_t)L.taps_b};
+        if (g_encode(&L.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CC3D_ERR_CUDA;
+    }
+    L.has_cache = cache_in != nullptr;
+    L.bias = b;
+    L.res = res;
+    L.y = y;
+    L.x = x;
+    L.cache_in = cache_in;
+    L.cache_out = cache_out;
+    L.status = d->status;
+    L.wait_ns = p.wait_ns;
+    L.fault = p.fault;
+    const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * T;
+    L.grid = ntiles < d->sms ? ntiles : d->sms;
+    return tc_launch(p.CB, L, stream) == cudaSuccess ? CC3D_OK : CC3D_ERR_CUDA;
+}
+
+}  // extern "C"

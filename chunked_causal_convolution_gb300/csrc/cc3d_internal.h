@@ -1,0 +1,86 @@
+// cc3d_internal.h -- launch descriptors shared between the C-ABI layer and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace cc3d {
+
+// Device status word bits (or-ed by kernels, read and cleared by cc3d_get_status).
+enum : unsigned {
+    STATUS_TIMEOUT_LOADER = 1u << 0,
+    STATUS_TIMEOUT_MMA = 1u << 1,
+    STATUS_TIMEOUT_EPILOGUE = 1u << 2,
+    STATUS_TIMEOUT_DRAIN = 1u << 3,
+};
+
+// Geometry of the tensor-core kernel's tiles.
+//
+// The frame is cut into column blocks of S pixels.  Inside a column block the
+// pixels are numbered in a "padded flat" order f = h * Sp + j with Sp = S + 2:
+// j = 0 and j = S + 1 are the zero columns left and right of the block, so
+// every spatial tap (dh, dw) of every output position f reads the input at
+// f + (dh - 1) * Sp + (dw - 1) -- a pure shift.  A tile is SUB groups of 128
+// consecutive output positions (one MMA row block each); in row-aligned mode
+// (S == 128) each group is exactly one row segment, otherwise groups are
+// consecutive 128-blocks of f and the positions on padding columns or beyond
+// the last row are computed but not stored.
+struct TcGeometry {
+    int S, Sp, ncolblk;
+    int row_aligned;
+    int sub;            // 128-row groups per tile
+    int sub_stride;     // f distance between groups (Sp or 128)
+    int tile_f;         // f distance between consecutive tiles of a column block
+    int tiles_per_cb;   // tiles per (frame, column block)
+    int nrows;          // padded rows loaded per input window
+};
+
+struct TcLaunch {
+    // tensor maps (encoded on the host)
+    CUtensorMap map_x;      // x_chunk   [T][H][W][Cin]   box (CB, Sp, nrows, 1)
+    CUtensorMap map_cache;  // cache_in  [P][H][W][Cin]   same box (unused if no cache)
+    CUtensorMap map_w;      // w viewed as (Cin, Cout, taps) box (CB, NT, taps_b)
+    int T, H, W, Cin, Cout;
+    int NT, nsplit, acc_stages, taps_b;
+    int na, nb;                       // A / B ring stages
+    int a_stage_bytes, b_stage_bytes;
+    int tmem_cols;                    // allocated columns (power of two)
+    TcGeometry g;
+    int has_cache;
+    const void* bias;                 // bf16 [Cout] or null
+    const void* res;                  // bf16 [T][H][W][Cout] or null
+    void* y;                          // bf16 [T][H][W][Cout]
+    // temporal cache update (done by otherwise idle warps)
+    const void* x;
+    const void* cache_in;
+    void* cache_out;
+    unsigned* status;
+    unsigned long long wait_ns;
+    int fault;
+    int grid;
+    size_t smem_bytes;
+};
+
+// Pick tiles / pipeline depths for a tensor-core launch.  Returns false if the
+// shape has no configuration.
+bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L);
+cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream);
+
+// fp32 direct kernel (CUDA cores, fixed accumulation order).
+struct SimtLaunch {
+    int T, H, W, Cin, Cout, kt, kh, kw;
+    const float* x;
+    const float* cache_in;
+    const float* w;
+    const float* bias;
+    const float* res;
+    float* y;
+};
+cudaError_t simt_f32_launch(const SimtLaunch& L, cudaStream_t stream);
+
+// cache_out[j] = frame (T + j) of concat(cache_in or zeros, x), j < P; plain 16-byte copies.
+cudaError_t cache_update_launch(const void* x, const void* cache_in, void* cache_out, int T, int P,
+                                size_t frame_bytes, cudaStream_t stream);
+cudaError_t zero_fill_launch(void* p, size_t bytes, cudaStream_t stream);
+
+}  // namespace cc3d

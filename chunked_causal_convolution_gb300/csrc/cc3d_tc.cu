@@ -1,0 +1,487 @@
+// cc3d_tc.cu -- implicit-GEMM causal 3x3x3 convolution on the sm_103a tensor cores.
+//
+// GEMM view: rows (M) = output positions of one frame, columns (N) = output
+// channels, reduction (K) = 27 taps x Cin.  Accumulators live in tensor memory
+// (fp32), operands are staged in shared memory by TMA:
+//
+//   * A: for every (temporal tap dt, channel block cb) one input window of
+//     `nrows` padded rows x Sp pixels x CB channels is loaded once; the nine
+//     spatial taps (dh, dw) of every 128-row group are row-shifted views of
+//     that window (see TcGeometry): the tensor core applies the swizzle on
+//     absolute shared-memory addresses, so a descriptor that starts any number
+//     of rows into the swizzled window is valid.  The TMA box starts one pixel
+//     left of the column block and may start above the frame; everything
+//     outside the frame is filled with zeros by the copy engine, which is the
+//     spatial zero padding.  Frames before the chunk come from the caller's
+//     cache (or read as zeros through a negative frame coordinate when there is
+//     no cache), which is the causal history.
+//   * B: the weights of `taps_b` taps for the same channel block, K-major.
+//
+// Warp roles (256 threads): warp 0 = TMA loader, warp 1 = MMA issuer, warp 2
+// = tensor-memory allocator and, with warp 3, the copy of the new temporal
+// cache, warps 4-7 = epilogue (tensor memory -> registers -> + bias
+// [+ residual] -> bf16 -> global), one output position per thread.
+//
+// The accumulation order of every output is fixed: dt, channel block, dh, dw,
+// 16-channel step -- it depends neither on the tile an output falls in nor on
+// how the video is cut into chunks, so chunked and unchunked results are
+// bit-identical.
+#include <cuda_bf16.h>
+
+#include "cc3d_internal.h"
+#include "cc3d_ptx.cuh"
+
+namespace cc3d {
+using namespace ptx;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxStages = 8;
+constexpr int kMaxAcc = 2;
+constexpr int kMaxSub = 4;
+
+struct TileCoord {
+    int t, w0, f0, hstart;
+};
+
+__device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+__device__ __forceinline__ TileCoord tile_coord(const TcLaunch& L, int tile)
+{
+    TileCoord c;
+    c.t = tile % L.T;
+    const int r = tile / L.T;
+    const int i = r % L.g.tiles_per_cb;
+    const int cbk = r / L.g.tiles_per_cb;
+    c.w0 = cbk * L.g.S;
+    c.f0 = i * L.g.tile_f + (L.g.row_aligned ? 1 : 0);
+    c.hstart = floor_div(c.f0 - L.g.Sp - 1, L.g.Sp);
+    return c;
+}
+
+__device__ __forceinline__ void record_failure(const TcLaunch& L, unsigned bit, volatile int* abort_flag)
+{
+    *abort_flag = 1;
+    atomicOr(L.status, bit);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat16 l = __float2bfloat16_rn(lo);
+    const __nv_bfloat16 h = __float2bfloat16_rn(hi);
+    return (uint32_t)__bfloat16_as_ushort(l) | ((uint32_t)__bfloat16_as_ushort(h) << 16);
+}
+
+template <int CB>
+__global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_constant__ TcLaunch L)
+{
+    constexpr uint32_t ROWB = CB * 2;  // bytes of one pixel row of a channel block = swizzle span
+    constexpr uint32_t LAYOUT = CB == 64 ? LAYOUT_SW128 : (CB == 32 ? LAYOUT_SW64 : LAYOUT_SW32);
+    constexpr uint32_t SBO = 8 * ROWB;
+    constexpr int KSTEPS = CB / 16;
+
+    extern __shared__ uint8_t dsm_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smA = sm;
+    uint8_t* smB = sm + (size_t)L.na * L.a_stage_bytes;
+    float* s_bias = reinterpret_cast<float*>(smB + (size_t)L.nb * L.b_stage_bytes);
+
+    __shared__ uint64_t a_full[kMaxStages], a_empty[kMaxStages], b_full[kMaxStages], b_empty[kMaxStages];
+    __shared__ uint64_t acc_full[kMaxAcc], acc_empty[kMaxAcc], mma_drain;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int Sp = L.g.Sp;
+    const int NT = L.NT;
+    const int nsplit = L.nsplit;
+    const int sub = L.g.sub;
+    const int ncb = L.Cin / CB;
+    const int bper = 9 / L.taps_b;  // B stages per (dt, cb)
+    const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * L.T;
+    const int cout_pad = nsplit * NT;
+    const uint32_t acc_cols = (uint32_t)(sub * nsplit * NT);
+    const unsigned long long budget = L.wait_ns;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < L.na; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], 1); }
+        for (int s = 0; s < L.nb; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 1); }
+        for (int a = 0; a < L.acc_stages; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 4); }
+        mbar_init(&mma_drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&L.map_x);
+        prefetch_tensormap(&L.map_w);
+        if (L.has_cache) prefetch_tensormap(&L.map_cache);
+    }
+    if (warp == 2) {
+        tmem_alloc(&tmem_base_sh, (uint32_t)L.tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp >= 4) {
+        const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(L.bias);
+        for (int i = threadIdx.x - 128; i < cout_pad; i += 128)
+            s_bias[i] = (b != nullptr && i < L.Cout) ? __bfloat162float(b[i]) : 0.0f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA loader
+        if (lane == 0) {
+            int sa = 0, pa = 0, sb = 0, pb = 0;
+            int last_pa[kMaxStages], last_pb[kMaxStages];
+            for (int s = 0; s < kMaxStages; ++s) last_pa[s] = last_pb[s] = -1;
+            const uint32_t a_tx = (uint32_t)(ROWB * Sp * L.g.nrows);
+            const uint32_t b_tx = (uint32_t)(ROWB * NT * L.taps_b * nsplit);
+            bool skip_first = (L.fault == 1);
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+                const TileCoord c = tile_coord(L, tile);
+                for (int dt = 0; ok && dt < 3; ++dt) {
+                    const int tin = c.t + dt - 2;
+                    const CUtensorMap* map = &L.map_x;
+                    int tc = tin;
+                    if (tin < 0 && L.has_cache) { map = &L.map_cache; tc = tin + 2; }
+                    for (int cb = 0; ok && cb < ncb; ++cb) {
+                        if (!bounded_wait(&a_empty[sa], pa ^ 1, budget, &abort_flag)) {
+                            if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&a_full[sa], a_tx);
+                        if (!skip_first)
+                            tma_load_4d(smA + (size_t)sa * L.a_stage_bytes, map, &a_full[sa], cb * CB, c.w0 - 1,
+                                        c.hstart, tc);
+                        skip_first = false;
+                        last_pa[sa] = pa;
+                        if (++sa == L.na) { sa = 0; pa ^= 1; }
+                        for (int tb = 0; tb < bper; ++tb) {
+                            if (!bounded_wait(&b_empty[sb], pb ^ 1, budget, &abort_flag)) {
+                                if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&b_full[sb], b_tx);
+                            const int tap0 = dt * 9 + tb * L.taps_b;
+                            uint8_t* dst = smB + (size_t)sb * L.b_stage_bytes;
+                            for (int ns = 0; ns < nsplit; ++ns)
+                                tma_load_3d(dst + (size_t)ns * L.taps_b * NT * ROWB, &L.map_w, &b_full[sb], cb * CB,
+                                            ns * NT, tap0);
+                            last_pb[sb] = pb;
+                            if (++sb == L.nb) { sb = 0; pb ^= 1; }
+                        }
+                    }
+                }
+            }
+            // never leave while a copy into this block's shared memory may still be in flight
+            for (int s = 0; s < L.na; ++s)
+                if (last_pa[s] >= 0 && !bounded_wait(&a_full[s], (uint32_t)last_pa[s], budget, nullptr))
+                    atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
+            for (int s = 0; s < L.nb; ++s)
+                if (last_pb[s] >= 0 && !bounded_wait(&b_full[s], (uint32_t)last_pb[s], budget, nullptr))
+                    atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc_bf16_f32(128, NT);
+            int sa = 0, pa = 0, sb = 0, pb = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+                const TileCoord c = tile_coord(L, tile);
+                const int as = it % L.acc_stages;
+                const int aph = (it / L.acc_stages) & 1;
+                if (!bounded_wait(&acc_empty[as], aph ^ 1, budget, &abort_flag)) {
+                    if (!abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dbase = tmem + (uint32_t)as * acc_cols;
+                int rowoff[kMaxSub];
+                for (int m = 0; m < kMaxSub; ++m) rowoff[m] = c.f0 + m * L.g.sub_stride - c.hstart * Sp - Sp - 1;
+                for (int dt = 0; ok && dt < 3; ++dt) {
+                    for (int cb = 0; ok && cb < ncb; ++cb) {
+                        if (!bounded_wait(&a_full[sa], pa, budget, &abort_flag)) {
+                            if (!abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t abase = smem_u32(smA + (size_t)sa * L.a_stage_bytes);
+                        for (int tb = 0; tb < bper; ++tb) {
+                            if (!bounded_wait(&b_full[sb], pb, budget, &abort_flag)) {
+                                if (!abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t bbase = smem_u32(smB + (size_t)sb * L.b_stage_bytes);
+                            for (int j = 0; j < L.taps_b; ++j) {
+                                const int tap = tb * L.taps_b + j;
+                                const int dh = tap / 3, dw = tap - 3 * (tap / 3);
+                                const int shift = dh * Sp + dw;
+                                for (int m = 0; m < sub; ++m) {
+                                    const uint32_t arow = abase + (uint32_t)(rowoff[m] + shift) * ROWB;
+#pragma unroll
+                                    for (int ks = 0; ks < KSTEPS; ++ks) {
+                                        const uint64_t ad = make_sdesc(arow + ks * 32, 16, SBO, LAYOUT, 0);
+                                        const uint32_t acc = (dt | cb | tap | ks) != 0;
+                                        for (int ns = 0; ns < nsplit; ++ns) {
+                                            const uint64_t bd = make_sdesc(
+                                                bbase + (uint32_t)((ns * L.taps_b + j) * NT) * ROWB + ks * 32, 16,
+                                                SBO, LAYOUT, 0);
+                                            umma_bf16_ss(dbase + (uint32_t)((m * nsplit + ns) * NT), ad, bd, idesc,
+                                                         acc);
+                                        }
+                                    }
+                                }
+                            }
+                            umma_commit(&b_empty[sb]);
+                            if (++sb == L.nb) { sb = 0; pb ^= 1; }
+                        }
+                        if (!ok) break;
+                        umma_commit(&a_empty[sa]);
+                        if (++sa == L.na) { sa = 0; pa ^= 1; }
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[as]);
+            }
+            // wait until every MMA this thread issued has finished writing tensor memory
+            umma_commit(&mma_drain);
+            if (!bounded_wait(&mma_drain, 0, budget, nullptr)) atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
+        }
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------------------------------ temporal cache update
+        // cache_out[j] = frame (T + j) of concat(cache_in, x); j < 2.
+        const size_t frame_chunks = (size_t)L.H * L.W * L.Cin * 2 / 16;
+        const size_t total = 2 * frame_chunks;
+        const size_t gthreads = (size_t)gridDim.x * 64;
+        const uint4* xin = reinterpret_cast<const uint4*>(L.x);
+        const uint4* cin = reinterpret_cast<const uint4*>(L.cache_in);
+        uint4* cout_ = reinterpret_cast<uint4*>(L.cache_out);
+        for (size_t i = (size_t)blockIdx.x * 64 + (threadIdx.x - 64); i < total; i += gthreads) {
+            const int j = (int)(i / frame_chunks);
+            const size_t o = i - (size_t)j * frame_chunks;
+            const int src = L.T + j;  // index in the extended stack
+            uint4 v;
+            if (src >= 2)
+                v = __ldg(xin + (size_t)(src - 2) * frame_chunks + o);
+            else if (cin != nullptr)
+                v = __ldg(cin + (size_t)src * frame_chunks + o);
+            else
+                v = make_uint4(0, 0, 0, 0);
+            cout_[i] = v;
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp - 4;  // tensor-memory lanes 32q .. 32q+31
+        const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(L.res);
+        __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(L.y);
+        const bool wide = (L.Cout % 16) == 0;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+            const int as = it % L.acc_stages;
+            const int aph = (it / L.acc_stages) & 1;
+            // one lane waits and the verdict is shared: tcgen05.ld below needs the whole warp
+            int ready = 0;
+            if (lane == 0) {
+                ready = bounded_wait(&acc_full[as], aph, budget, &abort_flag);
+                if (!ready && !abort_flag) record_failure(L, STATUS_TIMEOUT_EPILOGUE, &abort_flag);
+            }
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) break;
+            tc_fence_after();
+            const TileCoord c = tile_coord(L, tile);
+            for (int m = 0; m < sub; ++m) {
+                const int f = c.f0 + m * L.g.sub_stride + q * 32 + lane;
+                const int h = f / Sp;
+                const int jcol = f - h * Sp;
+                const int w = c.w0 + jcol - 1;
+                const bool valid = h < L.H && jcol >= 1 && jcol <= L.g.S && w < L.W;
+                const size_t px = ((size_t)c.t * L.H + (valid ? h : 0)) * L.W + (valid ? w : 0);
+                for (int ns = 0; ns < nsplit; ++ns) {
+                    for (int cc = 0; cc < NT; cc += 16) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
+                                               (uint32_t)((m * nsplit + ns) * NT + cc),
+                                           r);
+                        tmem_ld_wait();
+                        if (!valid) continue;
+                        const int co0 = ns * NT + cc;
+                        float v[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) v[k] = __fadd_rn(__uint_as_float(r[k]), s_bias[co0 + k]);
+                        if (wide) {
+                            const size_t off = px * L.Cout + co0;
+                            if (res != nullptr) {
+                                const uint4 r0 = __ldg(reinterpret_cast<const uint4*>(res + off));
+                                const uint4 r1 = __ldg(reinterpret_cast<const uint4*>(res + off + 8));
+                                const uint32_t rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) {
+                                    v[2 * k] = __fadd_rn(v[2 * k], bf16_lo(rr[k]));
+                                    v[2 * k + 1] = __fadd_rn(v[2 * k + 1], bf16_hi(rr[k]));
+                                }
+                            }
+                            uint4 o0, o1;
+                            o0.x = pack_bf16x2(v[0], v[1]);
+                            o0.y = pack_bf16x2(v[2], v[3]);
+                            o0.z = pack_bf16x2(v[4], v[5]);
+                            o0.w = pack_bf16x2(v[6], v[7]);
+                            o1.x = pack_bf16x2(v[8], v[9]);
+                            o1.y = pack_bf16x2(v[10], v[11]);
+                            o1.z = pack_bf16x2(v[12], v[13]);
+                            o1.w = pack_bf16x2(v[14], v[15]);
+                            *reinterpret_cast<uint4*>(y + off) = o0;
+                            *reinterpret_cast<uint4*>(y + off + 8) = o1;
+                        } else {
+                            // narrow output head: fewer than 16 channels, element stores
+                            for (int k = 0; k < 16; ++k) {
+                                const int co = co0 + k;
+                                if (co >= L.Cout) break;
+                                const size_t off = px * L.Cout + co;
+                                float o = v[k];
+                                if (res != nullptr) o = __fadd_rn(o, __bfloat162float(res[off]));
+                                y[off] = __float2bfloat16_rn(o);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[as]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem, (uint32_t)L.tmem_cols);
+}
+
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+int env_int(const char* name, int dflt)
+{
+    const char* s = getenv(name);
+    return (s != nullptr && *s) ? atoi(s) : dflt;
+}
+
+}  // namespace
+
+bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
+{
+    if (CB != 16 && CB != 32 && CB != 64) return false;
+    if (Cin % CB != 0) return false;
+    L->T = T;
+    L->H = H;
+    L->W = W;
+    L->Cin = Cin;
+    L->Cout = Cout;
+    // output channels per MMA (N) and number of N splits
+    if (Cout < 16) {
+        L->NT = 16;
+        L->nsplit = 1;
+    } else {
+        if (Cout % 16 != 0) return false;
+        int ns = cdiv(Cout, 256);
+        while (ns <= 4 && !(Cout % ns == 0 && (Cout / ns) % 16 == 0)) ++ns;
+        if (ns > 4) return false;
+        L->nsplit = ns;
+        L->NT = Cout / ns;
+    }
+    const int ntot = L->NT * L->nsplit;
+    // tensor-memory budget: sub * ntot * acc_stages <= 512 columns
+    int sub = 256 / ntot, acc = 2;
+    if (sub < 1) {
+        acc = 1;
+        sub = 512 / ntot;
+        if (sub < 1) return false;
+    }
+    if (sub > kMaxSub) sub = kMaxSub;
+    sub = env_int("CC3D_TC_SUB", sub);
+    acc = env_int("CC3D_TC_ACC", acc);
+    if (sub < 1 || sub > kMaxSub || acc < 1 || acc > kMaxAcc || sub * ntot * acc > 512) return false;
+    L->acc_stages = acc;
+    int cols = 32;
+    while (cols < sub * ntot * acc) cols *= 2;
+    L->tmem_cols = cols;
+    // column blocks and padded-flat geometry
+    TcGeometry& g = L->g;
+    g.sub = sub;
+    if (W % 128 == 0) {
+        g.S = 128;
+        g.row_aligned = 1;
+    } else {
+        const int nblk = cdiv(W, 254);
+        g.S = cdiv(W, nblk);
+        g.row_aligned = 0;
+    }
+    g.Sp = g.S + 2;
+    g.ncolblk = cdiv(W, g.S);
+    if (g.row_aligned) {
+        g.sub_stride = g.Sp;
+        g.tile_f = sub * g.Sp;
+        g.tiles_per_cb = cdiv(H, sub);
+        g.nrows = sub + 2;
+    } else {
+        g.sub_stride = 128;
+        g.tile_f = sub * 128;
+        g.tiles_per_cb = cdiv(H * g.Sp, g.tile_f);
+        // the last row any view reads is at most 3*Sp + sub*128 past the window start
+        g.nrows = 4 + (sub * 128) / g.Sp;
+    }
+    if (g.nrows > 256 || g.Sp > 256) return false;
+    // pipeline stages
+    const int rowb = CB * 2;
+    const int a_bytes = rowb * g.Sp * g.nrows;
+    L->a_stage_bytes = (a_bytes + 1023) & ~1023;
+    L->taps_b = (3 * ntot * rowb <= 40 * 1024) ? 3 : 1;
+    L->b_stage_bytes = (L->taps_b * ntot * rowb + 1023) & ~1023;
+    const int budget = 220 * 1024 - 4 * ntot;
+    L->na = (L->a_stage_bytes > 40 * 1024) ? 2 : 3;
+    L->na = env_int("CC3D_TC_NA", L->na);
+    if (L->na < 2 || L->na > kMaxStages) return false;
+    int nb = (budget - L->na * L->a_stage_bytes) / L->b_stage_bytes;
+    if (nb > kMaxStages) nb = kMaxStages;
+    if (nb < 2) {
+        L->na = 2;
+        nb = (budget - L->na * L->a_stage_bytes) / L->b_stage_bytes;
+        if (nb > kMaxStages) nb = kMaxStages;
+        if (nb < 2) return false;
+    }
+    L->nb = nb;
+    L->smem_bytes = (size_t)L->na * L->a_stage_bytes + (size_t)L->nb * L->b_stage_bytes + 4 * ntot + 1024;
+    // one block per SM: a second resident block would wait inside its tensor-memory allocation
+    if (L->smem_bytes < 120 * 1024) L->smem_bytes = 120 * 1024;
+    return true;
+}
+
+cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream)
+{
+    void (*kern)(TcLaunch) = nullptr;
+    if (CB == 16)
+        kern = tc_bf16_kernel<16>;
+    else if (CB == 32)
+        kern = tc_bf16_kernel<32>;
+    else
+        kern = tc_bf16_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem_bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<L.grid, kThreads, L.smem_bytes, stream>>>(L);
+    return cudaGetLastError();
+}
+
+}  // namespace cc3d

@@ -1,0 +1,143 @@
+/*
+ * cc3d.h -- C ABI of the chunked causal 3-D convolution library (libcc3d.so).
+ *
+ * The operation (NDHWC activations, batch 1):
+ *
+ *   y[t,h,w,co] = b[co] + sum_{dt<kt, dh<kh, dw<kw, ci<Cin}
+ *                   w[co,dt,dh,dw,ci] * xe[t+dt, h+dh-(kh-1)/2, w+dw-(kw-1)/2, ci]
+ *                 (+ residual[t,h,w,co])
+ *
+ *   xe = concat_t(cache_in, x_chunk) is the chunk preceded by the kt-1 input
+ *   frames of the previous chunk (all zeros for the first chunk of a video);
+ *   spatial positions outside the frame read zero.  After the call,
+ *   cache_out holds the last kt-1 frames of xe, which is the history the next
+ *   chunk needs.
+ *
+ * Sources: "SwiftVR Inference Optimization" (LightX2V blog), section "ReAE:
+ * Causal Halo Exchange" -- a causal layer convolves the current frame's input
+ * features together with the preceding frames' input features; across chunks
+ * only the previous chunk's last input frames are carried; the first chunk of
+ * a video uses zeros as its history.  Section "From Pixels to Latents and
+ * Back" -- long videos are processed in temporal chunks while the per-layer
+ * boundary features are kept.  "SGLang-Diffusion advanced optimizations",
+ * section 3 "Parallel VAE" -- the VAE's cost is dense 3-D convolution, and
+ * chunked or halo-split evaluation must stay equal to the unsplit result.
+ * The state conventions (validate everything before touching any buffer,
+ * caller-owned state buffers that swap roles between calls, reset without
+ * reallocation, one instance per shape, no host synchronisation per call)
+ * follow the "pixtreme-infer-cda-vsr" package page, section "Frame, state and
+ * stream requirements" and "CUDA Graph inference".
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never frees, retains or reallocates them.  They must be 16-byte aligned
+ *    for bfloat16 plans (tensor-memory-accelerator copies) and 4-byte aligned
+ *    for float32 plans.
+ *  - Layouts are dense row-major (channels innermost):
+ *      x_chunk, residual, y : [T_chunk][H][W][C]
+ *      cache_in, cache_out  : [kt-1][H][W][Cin]
+ *      w                    : [Cout][kt][kh][kw][Cin]
+ *      b                    : [Cout]
+ *    with the element type of the plan (float32 or bfloat16) for all of them.
+ *  - Work is enqueued on the given CUDA stream (a cudaStream_t passed as
+ *    void*; NULL means the legacy default stream).  No call except
+ *    cc3d_get_status synchronises the host.
+ *  - Every argument is checked before anything is launched or written; a
+ *    failed check returns an error code and leaves every buffer untouched.
+ *  - Kernel waits are bounded.  A wait that runs out records an error in a
+ *    per-device status word and the kernel returns; cc3d_get_status reports
+ *    it.
+ */
+#ifndef CC3D_H
+#define CC3D_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct cc3d_plan_s* cc3d_plan_t; /* opaque, owned by the library */
+
+typedef enum { CC3D_F32 = 0, CC3D_BF16 = 1 } cc3d_dtype;
+
+typedef enum {
+    CC3D_OK = 0,
+    CC3D_ERR_INVALID_ARG = 1,     /* null / negative / inconsistent argument        */
+    CC3D_ERR_UNSUPPORTED = 2,     /* shape or dtype this build has no kernel for     */
+    CC3D_ERR_ALIGNMENT = 3,       /* pointer not aligned (16 B bf16, 4 B fp32)       */
+    CC3D_ERR_ALIAS = 4,           /* an output overlaps another buffer              */
+    CC3D_ERR_CUDA = 5,            /* a CUDA runtime call failed                     */
+    CC3D_ERR_OOM = 6,             /* host allocation failed                         */
+    CC3D_ERR_DEVICE_TIMEOUT = 7,  /* a bounded wait inside a kernel ran out          */
+    CC3D_ERR_NOT_DEVICE_MEMORY = 8 /* a tensor pointer is not device-accessible       */
+} cc3d_status;
+
+/*
+ * Create a plan for one layer shape.  Host-only: no CUDA call, no device
+ * allocation.  kh and kw must be odd.  Supported in this build:
+ *   CC3D_F32  : any Cin, Cout >= 1; 1 <= kt <= 4; kh, kw in {1, 3, 5}.
+ *   CC3D_BF16 : kt = kh = kw = 3, Cin a multiple of 16 (<= 1024), Cout a
+ *               multiple of 16 (<= 512) or Cout < 16 (narrow output head).
+ * Anything else returns CC3D_ERR_UNSUPPORTED.  On error *out is set to NULL
+ * and nothing is leaked.
+ */
+cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, int kw, cc3d_dtype dtype,
+                             cc3d_plan_t* out);
+
+/*
+ * One temporal chunk of T_chunk frames (see the formula above).
+ *   x_chunk  [T_chunk][H][W][Cin]  input frames of this chunk.
+ *   w, b     weights and bias; b may be NULL (zero bias).
+ *   residual [T_chunk][H][W][Cout] added after the bias, or NULL.
+ *   cache_in [kt-1][H][W][Cin] history, or NULL for zero history (first chunk).
+ *   cache_out[kt-1][H][W][Cin] receives the new history.  It must not overlap
+ *            cache_in, x_chunk, y or residual (ping-pong two buffers).
+ *   y        [T_chunk][H][W][Cout] output; must not overlap any input.
+ * T_chunk may be 0: then only cache_out is written (it receives cache_in, or
+ * zeros), and x_chunk, residual and y may be NULL.
+ * The result of every output element does not depend on how the video is
+ * split into chunks (bit-identical across chunkings).
+ * Returns CC3D_OK once the work is enqueued; asynchronous failures surface in
+ * cc3d_get_status.
+ */
+cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T_chunk, const void* x_chunk, const void* w, const void* b,
+                               const void* residual_or_null, const void* cache_in, void* cache_out, void* y,
+                               void* stream);
+
+/* Zero a cache buffer ([kt-1][H][W][Cin]) on the stream: the history of a new
+ * video.  Stream-ordered, no allocation.  Same alignment rule as the tensors. */
+cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream);
+
+/* Synchronise the stream, then report (and clear) the device status word and
+ * any pending CUDA error: CC3D_OK, CC3D_ERR_DEVICE_TIMEOUT or CC3D_ERR_CUDA. */
+cc3d_status cc3d_get_status(cc3d_plan_t plan, void* stream);
+
+/* Release the plan (NULL is accepted). */
+void cc3d_destroy(cc3d_plan_t plan);
+
+/* Static, human-readable text of a status code. */
+const char* cc3d_status_string(cc3d_status s);
+
+/* Name of the kernel family the plan will launch ("tc_bf16", "tc_bf16_narrow",
+ * "simt_f32"); a static string, NULL for a NULL plan. */
+const char* cc3d_plan_kernel(cc3d_plan_t plan);
+
+/* Number of kernel launches one cc3d_forward_chunk call of this plan makes
+ * (T_chunk >= 1). */
+int cc3d_plan_launches_per_chunk(cc3d_plan_t plan);
+
+/*
+ * Test hooks (used by the fault tests; never needed in normal use).
+ * cc3d_debug_set_wait_budget_ns: wall-clock budget of every bounded wait in
+ *   this plan's kernels (default 2e9 ns).
+ * cc3d_debug_set_fault: 0 = none; 1 = the tensor-core kernel's loader skips
+ *   its first copy so that the consumer's bounded wait runs out (the kernel
+ *   then records CC3D_ERR_DEVICE_TIMEOUT and returns); 2 = fail host-side
+ *   tensor-map encoding (CC3D_ERR_CUDA, nothing launched).
+ */
+cc3d_status cc3d_debug_set_wait_budget_ns(cc3d_plan_t plan, unsigned long long ns);
+cc3d_status cc3d_debug_set_fault(cc3d_plan_t plan, int mode);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CC3D_H */

@@ -1,0 +1,117 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared symbol, and
+rejects bad arguments before touching any buffer (argument checks run on the host)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_causal_convolution_gb300 as cc3d
+from chunked_causal_convolution_gb300 import build as lib_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "cc3d.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return cc3d.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cc3d_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for n in ("cc3d_plan_create", "cc3d_forward_chunk", "cc3d_reset", "cc3d_destroy", "cc3d_get_status"):
+        assert n in names
+    assert set(names) == set(cc3d.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = cc3d.cc3d_status_string(code)
+        assert s and s != "unknown status"
+    assert cc3d.cc3d_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 16, 8, 8, 3, 3, 3, cc3d.CC3D_BF16), 1),
+    ((16, 16, 8, 0, 3, 3, 3, cc3d.CC3D_BF16), 1),
+    ((16, 16, 8, 8, 3, 2, 3, cc3d.CC3D_BF16), 1),    # even spatial extent
+    ((16, 16, 8, 8, 3, 3, 3, 7), 1),                 # unknown dtype
+    ((24, 16, 8, 8, 3, 3, 3, cc3d.CC3D_BF16), 2),    # Cin not a multiple of 16
+    ((32, 24, 8, 8, 3, 3, 3, cc3d.CC3D_BF16), 2),    # Cout >= 16 not a multiple of 16
+    ((32, 32, 8, 8, 2, 3, 3, cc3d.CC3D_BF16), 2),    # bf16 needs 3x3x3 in this build
+    ((32, 1024, 8, 8, 3, 3, 3, cc3d.CC3D_BF16), 2),  # beyond tensor-memory budget
+    ((4, 4, 8, 8, 5, 3, 3, cc3d.CC3D_F32), 2),       # fp32 temporal extent limit
+])
+def test_plan_create_rejects(lib, args, code):
+    h = ctypes.c_void_p(123)
+    rc = lib.cc3d_plan_create(*args, ctypes.byref(h))
+    assert rc == code
+    assert h.value is None  # *out is cleared on error
+
+
+@pytest.mark.parametrize("args,kernel,launches", [
+    ((96, 96, 360, 640, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
+    ((384, 384, 90, 160, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
+    ((96, 3, 1440, 2560, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),
+    ((16, 16, 32, 32, 3, 3, 3, cc3d.CC3D_F32), "simt_f32", 2),
+    ((3, 5, 7, 9, 2, 1, 3, cc3d.CC3D_F32), "simt_f32", 2),
+])
+def test_plan_create_accepts(lib, args, kernel, launches):
+    p = cc3d.cc3d_plan_create(*args)
+    try:
+        assert cc3d.cc3d_plan_kernel(p) == kernel
+        assert cc3d.cc3d_plan_launches_per_chunk(p) == launches
+    finally:
+        cc3d.cc3d_destroy(p)
+
+
+def test_destroy_null_is_safe(lib):
+    lib.cc3d_destroy(None)
+
+
+def test_forward_rejects_before_any_device_work(lib):
+    p = cc3d.cc3d_plan_create(32, 32, 4, 8, 3, 3, 3, cc3d.CC3D_BF16)
+    try:
+        # x 2 KB, w 54 KB, y 2 KB, caches 4 KB each: disjoint spans in one host buffer
+        buf = (ctypes.c_uint8 * (1 << 17))()
+        base = (ctypes.addressof(buf) + 255) & ~255
+        x, w, y, c0, c1 = base, base + 4096, base + 65536, base + 69632, base + 77824
+        f = lib.cc3d_forward_chunk
+        assert f(None, 1, x, w, None, None, None, c1, y, None) == 1          # null plan
+        assert f(p, -1, x, w, None, None, None, c1, y, None) == 1            # negative T
+        assert f(p, 1, None, w, None, None, None, c1, y, None) == 1          # missing x
+        assert f(p, 1, x, w, None, None, None, None, y, None) == 1           # missing cache_out
+        assert f(p, 1, x + 8, w, None, None, None, c1, y, None) == 3         # misaligned
+        assert f(p, 1, x, w, None, None, None, c1, x, None) == 4             # y overlaps x
+        assert f(p, 1, x, w, None, None, c0, c0, y, None) == 4               # cache_out overlaps cache_in
+        assert f(p, 1, x, w, None, None, None, x, y, None) == 4              # cache_out overlaps x
+        # host memory is not device memory (no GPU here: the check itself fails closed)
+        assert f(p, 1, x, w, None, None, None, c1, y, None) == 8
+        assert lib.cc3d_reset(p, base + 8, None) == 3
+        assert lib.cc3d_reset(None, base, None) == 1
+        assert lib.cc3d_debug_set_fault(p, 9) == 1
+        assert lib.cc3d_debug_set_wait_budget_ns(p, 0) == 1
+    finally:
+        cc3d.cc3d_destroy(p)
+
+
+def test_binding_raises_loudly_without_the_library(monkeypatch, tmp_path):
+    import importlib
+    mod = importlib.import_module("chunked_causal_convolution_gb300")
+    monkeypatch.setattr(mod, "_lib", None)
+    monkeypatch.setattr(mod, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        mod.cc3d_plan_create(16, 16, 8, 8)

@@ -1,0 +1,338 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
+
+* small shapes compared element by element (several tiles, ragged tails, every
+  kernel family: tensor-core row-aligned / flat / split-N / narrow head /
+  16-channel blocks, and the fp32 CUDA-core path including the tiny fp32
+  workload itself);
+* the decoder-shaped workloads at full size, in the launch configuration the
+  benchmark times (chunks of 4 frames with a carried cache), compared on
+  sampled outputs (random positions, frame borders, chunk seams, column-block
+  seams) that the oracle evaluates one by one;
+* bit-identity of the GPU result across chunkings;
+* tolerances: bf16  max|err| <= 2e-2 * RMS(y_oracle) over the compared set,
+             fp32  max|err| <= 1e-4 * max|y_oracle|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import chunked_causal_convolution_gb300 as cc3d
+import oracle
+import synth
+from synth import native
+from tests.helpers import (compositions_sample, from_device, run_chunks, small_inputs, to_device, to_f64,
+                           tolerance)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+SMALL = [
+    # name, dtype, Cin, Cout, T, H, W, chunks, bias, residual
+    ("tiny_f32_workload", "f32", 16, 16, 8, 32, 32, [4, 4], True, False),
+    ("f32_odd_shape", "f32", 3, 5, 5, 7, 9, [2, 1, 2], True, True),
+    ("bf16_row_aligned_residual", "bf16", 96, 96, 5, 5, 256, [2, 3], True, True),
+    ("bf16_flat", "bf16", 64, 64, 3, 7, 100, [1, 2], True, False),
+    ("bf16_split_n", "bf16", 32, 384, 3, 4, 40, [3], False, True),
+    ("bf16_narrow_head", "bf16", 96, 3, 3, 6, 130, [2, 1], True, True),
+    ("bf16_cb16", "bf16", 16, 32, 4, 9, 17, [1, 1, 2], True, False),
+    ("bf16_two_flat_blocks", "bf16", 32, 16, 2, 3, 300, [2], True, False),
+    ("bf16_c192_like", "bf16", 192, 192, 3, 8, 64, [2, 1], True, False),
+    ("bf16_one_pixel", "bf16", 32, 32, 3, 1, 1, [1, 1, 1], True, True),
+]
+
+
+def _small_case(name, dtype, Cin, Cout, T, H, W, chunks, bias, residual):
+    x_dist = synth.Dist.uniform(-1.0, 1.0) if name == "tiny_f32_workload" else None
+    seed = 0 if name == "tiny_f32_workload" else 100 + len(name)
+    raw = small_inputs(Cin, Cout, T, H, W, dtype, seed, bias, residual, x_dist=x_dist)
+    dev = {k: to_device(v, dtype) for k, v in raw.items()}
+    plan = cc3d.CausalConv3dPlan(Cin, Cout, H, W, dtype=dtype)
+    return raw, dev, plan
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_shapes_match_oracle_elementwise(case):
+    name, dtype, Cin, Cout, T, H, W, chunks, bias, residual = case
+    raw, dev, plan = _small_case(*case)
+    y, caches = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), chunks)
+    assert plan.status() == 0
+    ref = oracle.conv_whole(to_f64(raw["x"], dtype), to_f64(raw["w"], dtype),
+                            to_f64(raw["b"], dtype) if bias else None,
+                            to_f64(raw["r"], dtype) if residual else None)
+    got = from_device(y)
+    err = np.abs(got - ref).max()
+    assert err <= tolerance(dtype, ref), (name, err, tolerance(dtype, ref))
+    # every cache_out holds the two input frames preceding the next chunk, bit for bit
+    xs = dev["x"]
+    end = 0
+    for c, cache in zip(chunks, caches):
+        end += c
+        for j in range(2):
+            src = end - 2 + j
+            exp = xs[src] if src >= 0 else torch.zeros_like(xs[0])
+            assert torch.equal(cache[j], exp), (name, end, j)
+    # bit-identical across chunkings
+    for alt in ([T], [1] * T):
+        y2, _ = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), alt)
+        assert torch.equal(y2, y), (name, alt)
+    plan.close()
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def _gpu_inputs(wl, T=None, with_x=True):
+    """Full tensors generated on the device from the shared counter-based generator."""
+    T = T or wl.T
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    d = {}
+    if with_x:
+        d["x"] = native.fill_device(torch.empty((T, wl.H, wl.W, wl.Cin), dtype=dt, device="cuda"), wl.seed,
+                                    synth.TID_X, wl.x)
+    d["w"] = native.fill_device(torch.empty((wl.Cout, 3, 3, 3, wl.Cin), dtype=dt, device="cuda"), wl.seed,
+                                synth.TID_W, wl.w)
+    if wl.b is not None:
+        d["b"] = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device="cuda"), wl.seed, synth.TID_B, wl.b)
+    if wl.r is not None:
+        d["r"] = native.fill_device(torch.empty((T, wl.H, wl.W, wl.Cout), dtype=dt, device="cuda"), wl.seed,
+                                    synth.TID_R, wl.r)
+    return d
+
+
+def _sample_points(wl, T, seams, rng, n_random):
+    H, W = wl.H, wl.W
+    pts = set()
+    for _ in range(n_random):
+        pts.add((int(rng.integers(T)), int(rng.integers(H)), int(rng.integers(W))))
+    frames = sorted(f for f in ({0, 1, 2, T - 1} | set(seams) | set(s - 1 for s in seams)) if 0 <= f < T)
+    cols = sorted({0, 1, W - 2, W - 1} | {c for c in (127, 128, 129, 159, 160, 161, 255, 256) if c < W})
+    rows = sorted({0, 1, H - 2, H - 1} | {H // 2})
+    for t in frames:
+        for h in rows:
+            for w in cols:
+                pts.add((t, h, w))
+        for _ in range(24):
+            pts.add((t, int(rng.integers(H)), int(rng.integers(W))))
+    return np.array(sorted(pts), dtype=np.int64)
+
+
+def _windows(wl, pts):
+    """Input values around each point, from the host copy of the generator (out-of-video entries
+    are computed at clamped coordinates and ignored by the oracle)."""
+    H, W, C = wl.H, wl.W, wl.Cin
+    dt_, dh_, dw_ = np.meshgrid(np.arange(3), np.arange(3), np.arange(3), indexing="ij")
+    t = np.maximum(pts[:, 0, None, None, None] + dt_ - 2, 0)
+    h = np.clip(pts[:, 1, None, None, None] + dh_ - 1, 0, H - 1)
+    w = np.clip(pts[:, 2, None, None, None] + dw_ - 1, 0, W - 1)
+    base = ((t * H + h) * W + w) * C
+    e = base[..., None] + np.arange(C)
+    raw = native.values_host(wl.seed, synth.TID_X, wl.x, e, wl.dtype)
+    return to_f64(raw, wl.dtype)
+
+
+def _oracle_at(wl, T, pts):
+    e_w = synth.dense_index((wl.Cout, 3, 3, 3, wl.Cin))
+    w = to_f64(native.values_host(wl.seed, synth.TID_W, wl.w, e_w, wl.dtype), wl.dtype)
+    b = None if wl.b is None else to_f64(native.values_host(wl.seed, synth.TID_B, wl.b,
+                                                            np.arange(wl.Cout), wl.dtype), wl.dtype)
+    r = None
+    if wl.r is not None:
+        e_r = (((pts[:, 0] * wl.H + pts[:, 1]) * wl.W + pts[:, 2]) * wl.Cout)[:, None] + np.arange(wl.Cout)
+        r = to_f64(native.values_host(wl.seed, synth.TID_R, wl.r, e_r, wl.dtype), wl.dtype)
+    return oracle.conv_points((T, wl.H, wl.W), pts, _windows(wl, pts), w, b, r)
+
+
+def _gather(y, pts):
+    idx = torch.from_numpy(pts).to(y.device)
+    return from_device(y[idx[:, 0], idx[:, 1], idx[:, 2]])
+
+
+FULL = ["c96_residual", "c192", "c384", "c384_to_192"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_sampled(name):
+    wl = synth.WORKLOADS[name]
+    d = _gpu_inputs(wl)
+    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, wl.H, wl.W, dtype=wl.dtype)
+    y, _ = run_chunks(plan, d["x"], d["w"], d.get("b"), d.get("r"), list(wl.chunks))
+    assert plan.status() == 0
+    seams = np.cumsum(wl.chunks)[:-1].tolist()
+    rng = np.random.default_rng(wl.seed)
+    n_random = int(min(4096, 6e6 / (27 * wl.Cin)))
+    pts = _sample_points(wl, wl.T, seams, rng, n_random)
+    ref = _oracle_at(wl, wl.T, pts)
+    got = _gather(y, pts)
+    err = np.abs(got - ref).max()
+    tol = tolerance(wl.dtype, ref)
+    assert err <= tol, (name, err, tol, len(pts))
+    # the same video cut differently gives the same bits
+    for parts in compositions_sample():
+        y2, _ = run_chunks(plan, d["x"], d["w"], d.get("b"), d.get("r"), parts)
+        assert torch.equal(y2, y), (name, parts)
+    plan.close()
+
+
+@pytest.mark.parametrize("name", ["sr96", "sr_head3"])
+def test_super_resolution_stream_sampled(name):
+    """The 361-frame 1440x2560 stream in 90 chunks of 4 and a last chunk of 1, the cache carried by
+    the library from chunk to chunk; outputs sampled in several chunks including the last."""
+    wl = synth.WORKLOADS[name]
+    d = _gpu_inputs(wl, with_x=False)
+    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, wl.H, wl.W, dtype=wl.dtype)
+    x = torch.empty((4, wl.H, wl.W, wl.Cin), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((4, wl.H, wl.W, wl.Cout), dtype=torch.bfloat16, device="cuda")
+    caches = [plan.new_cache(), plan.new_cache()]
+    frame = wl.H * wl.W * wl.Cin
+    check = {0, 1, 45, len(wl.chunks) - 2, len(wl.chunks) - 1}
+    rng = np.random.default_rng(wl.seed)
+    got_all, pts_all = [], []
+    s = 0
+    for k, c in enumerate(wl.chunks):
+        xc, yc = x[:c], y[:c]
+        native.fill_device(xc, wl.seed, synth.TID_X, wl.x, offset=s * frame)
+        plan.forward_chunk(xc, d["w"], d.get("b"), None, caches[k % 2] if k else None, caches[(k + 1) % 2], yc)
+        if k in check:
+            pts = _sample_points(wl, c, [], rng, 160)
+            got_all.append(_gather(yc, pts))
+            pts[:, 0] += s
+            pts_all.append(pts)
+        s += c
+    assert s == wl.T
+    assert plan.status() == 0
+    pts = np.concatenate(pts_all)
+    ref = _oracle_at(wl, wl.T, pts)
+    got = np.concatenate(got_all)
+    err = np.abs(got - ref).max()
+    assert err <= tolerance(wl.dtype, ref), (name, err, tolerance(wl.dtype, ref))
+    # the final history is the video's last two input frames
+    last = caches[len(wl.chunks) % 2]
+    exp = torch.empty_like(last)
+    native.fill_device(exp, wl.seed, synth.TID_X, wl.x, offset=(wl.T - 2) * frame)
+    assert torch.equal(last, exp)
+    plan.close()
+
+
+# ---------------------------------------------------------------- edge cases and contract
+
+def _tiny_bf16(T=4, H=6, W=40, C=32, residual=True, seed=7):
+    raw = small_inputs(C, C, T, H, W, "bf16", seed, True, residual)
+    return raw, {k: to_device(v, "bf16") for k, v in raw.items()}, cc3d.CausalConv3dPlan(C, C, H, W)
+
+
+def test_empty_chunk_passes_history_through():
+    raw, d, plan = _tiny_bf16()
+    cin = d["x"][:2].clone()
+    cout = plan.new_cache()
+    cc3d.cc3d_forward_chunk(plan.handle, 0, None, d["w"], d["b"], None, cin, cout, None)
+    torch.cuda.synchronize()
+    assert torch.equal(cout, cin)
+    cc3d.cc3d_forward_chunk(plan.handle, 0, None, d["w"], d["b"], None, None, cout, None)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(cout.float()) == 0
+    assert plan.status() == 0
+
+
+def test_zero_history_buffer_equals_null_history():
+    raw, d, plan = _tiny_bf16()
+    y0, _ = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [2, 2])
+    y1, _ = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [2, 2], zero_cache_first=True)
+    assert torch.equal(y0, y1)
+
+
+def test_single_frame_chunk_takes_history_from_cache():
+    raw, d, plan = _tiny_bf16()
+    _, caches = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [3, 1])
+    assert torch.equal(caches[1][0], d["x"][2]) and torch.equal(caches[1][1], d["x"][3])
+    _, caches = run_chunks(plan, d["x"][:1], d["w"], d["b"], d["r"][:1], [1])
+    assert torch.count_nonzero(caches[0][0].float()) == 0 and torch.equal(caches[0][1], d["x"][0])
+
+
+def test_optional_bias_and_residual():
+    raw, d, plan = _tiny_bf16(residual=False)
+    y, _ = run_chunks(plan, d["x"], d["w"], None, None, [4])
+    ref = oracle.conv_whole(to_f64(raw["x"], "bf16"), to_f64(raw["w"], "bf16"))
+    assert np.abs(from_device(y) - ref).max() <= tolerance("bf16", ref)
+
+
+def test_rejected_calls_leave_buffers_untouched():
+    raw, d, plan = _tiny_bf16()
+    y = torch.full((4, 6, 40, 32), 7.0, dtype=torch.bfloat16, device="cuda")
+    cout = torch.full((2, 6, 40, 32), 5.0, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cc3d.CC3DError) as e:
+        cc3d.cc3d_forward_chunk(plan.handle, 4, d["x"], d["w"], d["b"], None, None, d["x"][2:], y)
+    assert e.value.code == 4
+    with pytest.raises(cc3d.CC3DError) as e:
+        cc3d.cc3d_forward_chunk(plan.handle, 4, d["x"], d["w"], d["b"], y, None, cout, y)
+    assert e.value.code == 4
+    host = torch.zeros((4, 6, 40, 32), dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(cc3d.CC3DError) as e:
+        cc3d.cc3d_forward_chunk(plan.handle, 4, host.data_ptr(), d["w"], d["b"], None, None, cout, y)
+    assert e.value.code == 8
+    torch.cuda.synchronize()
+    assert torch.all(y.float() == 7.0) and torch.all(cout.float() == 5.0)
+
+
+def test_reset_zeroes_a_cache():
+    _, _, plan = _tiny_bf16()
+    c = torch.full((2, 6, 40, 32), 3.0, dtype=torch.bfloat16, device="cuda")
+    plan.reset(c)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(c.float()) == 0
+
+
+def test_resume_from_a_saved_history_is_bit_identical():
+    raw, d, plan = _tiny_bf16(T=6)
+    y_ref, caches = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [2, 2, 2])
+    saved = caches[1].cpu()  # history after chunk 2 (frames 2..3)
+    plan.close()
+    plan2 = cc3d.CausalConv3dPlan(32, 32, 6, 40)
+    cin = saved.cuda()
+    cout = plan2.new_cache()
+    y3 = plan2.forward_chunk(d["x"][4:], d["w"], d["b"], d["r"][4:], cin, cout)
+    assert torch.equal(y3, y_ref[4:])
+
+
+def test_non_default_stream():
+    raw, d, plan = _tiny_bf16()
+    y_ref, _ = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [4])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y_s, _ = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [4], stream=s)
+    s.synchronize()
+    assert torch.equal(y_s, y_ref)
+
+
+def test_bounded_wait_times_out_and_the_context_survives():
+    """The loader skips its first copy (test hook), the MMA warp's bounded wait runs out, the kernel
+    records a timeout and returns; the next call on the same context is correct."""
+    raw, d, plan = _tiny_bf16()
+    y_ref, _ = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [4])
+    plan.set_wait_budget_ns(50_000_000)
+    plan.set_fault(1)
+    y = torch.empty_like(y_ref)
+    cout = plan.new_cache()
+    plan.forward_chunk(d["x"], d["w"], d["b"], d["r"], None, cout, y)
+    assert plan.status() == 7
+    plan.set_fault(0)
+    y2, _ = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [4])
+    assert plan.status() == 0
+    assert torch.equal(y2, y_ref)
+
+
+def test_injected_host_encode_failure_launches_nothing():
+    raw, d, plan = _tiny_bf16()
+    plan.set_fault(2)
+    y = torch.full((4, 6, 40, 32), 9.0, dtype=torch.bfloat16, device="cuda")
+    cout = plan.new_cache()
+    with pytest.raises(cc3d.CC3DError) as e:
+        plan.forward_chunk(d["x"], d["w"], d["b"], d["r"], None, cout, y)
+    assert e.value.code == 5
+    torch.cuda.synchronize()
+    assert torch.all(y.float() == 9.0)

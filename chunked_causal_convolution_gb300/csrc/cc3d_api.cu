@@ -107,7 +107,7 @@ const char* cc3d_status_string(cc3d_status s)
     case CC3D_OK: return "ok";
     case CC3D_ERR_INVALID_ARG: return "invalid argument";
     case CC3D_ERR_UNSUPPORTED: return "unsupported shape, dtype or device";
-    case CC3D_ERR_ALIGNMENT: return "pointer not aligned (16 bytes for bf16, 4 for fp32)";
+    case CC3D_ERR_ALIGNMENT: return "pointer not aligned as the plan requires";
     case CC3D_ERR_ALIAS: return "output buffer overlaps another buffer";
     case CC3D_ERR_CUDA: return "CUDA runtime error";
     case CC3D_ERR_OOM: return "out of host memory";
@@ -242,11 +242,21 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     if (P > 0 && cache_out == nullptr) return CC3D_ERR_INVALID_ARG;
     if (T > 0 && (x == nullptr || w == nullptr || y == nullptr)) return CC3D_ERR_INVALID_ARG;
     if ((long long)T * p.H * p.W > (1LL << 40)) return CC3D_ERR_UNSUPPORTED;
-    // ---- alignment: 16 bytes for the tensor-core path (TMA), one element for fp32
-    const uintptr_t align = p.dtype == CC3D_F32 ? 4 : 16;
+    // ---- alignment.  fp32: one element.  bf16: 16 bytes for everything the tensor-core kernel
+    // moves with TMA or 16-byte vectors (x, w, caches, and y / residual when Cout is a multiple
+    // of 16); the narrow head stores y and reads the residual and bias per element.
     const void* all[] = {x, w, b, res, cache_in, cache_out, y};
-    for (const void* q : all)
-        if (q != nullptr && !aligned_to(q, align)) return CC3D_ERR_ALIGNMENT;
+    if (p.dtype == CC3D_F32) {
+        for (const void* q : all)
+            if (q != nullptr && !aligned_to(q, 4)) return CC3D_ERR_ALIGNMENT;
+    } else {
+        const uintptr_t out_align = (p.Cout % 16 == 0) ? 16 : 2;
+        const void* a16[] = {x, w, cache_in, cache_out};
+        for (const void* q : a16)
+            if (q != nullptr && !aligned_to(q, 16)) return CC3D_ERR_ALIGNMENT;
+        if ((y && !aligned_to(y, out_align)) || (res && !aligned_to(res, out_align)) || (b && !aligned_to(b, 2)))
+            return CC3D_ERR_ALIGNMENT;
+    }
     // ---- overlaps: outputs against everything else
     struct Span {
         const void* p;

@@ -30,9 +30,11 @@
  *
  * Conventions shared by every entry point
  *  - All tensor pointers are DEVICE pointers owned by the caller; the library
- *    never frees, retains or reallocates them.  They must be 16-byte aligned
- *    for bfloat16 plans (tensor-memory-accelerator copies) and 4-byte aligned
- *    for float32 plans.
+ *    never frees, retains or reallocates them.  Alignment: float32 plans need
+ *    4 bytes for every pointer; bfloat16 plans need 16 bytes for x_chunk, w,
+ *    cache_in and cache_out (tensor-memory-accelerator copies), 16 bytes for
+ *    y and residual when Cout is a multiple of 16 (2 bytes for the narrow
+ *    head, Cout < 16), and 2 bytes for b.
  *  - Layouts are dense row-major (channels innermost):
  *      x_chunk, residual, y : [T_chunk][H][W][C]
  *      cache_in, cache_out  : [kt-1][H][W][Cin]
@@ -63,7 +65,7 @@ typedef enum {
     CC3D_OK = 0,
     CC3D_ERR_INVALID_ARG = 1,     /* null / negative / inconsistent argument        */
     CC3D_ERR_UNSUPPORTED = 2,     /* shape or dtype this build has no kernel for     */
-    CC3D_ERR_ALIGNMENT = 3,       /* pointer not aligned (16 B bf16, 4 B fp32)       */
+    CC3D_ERR_ALIGNMENT = 3,       /* pointer not aligned (see Conventions)          */
     CC3D_ERR_ALIAS = 4,           /* an output overlaps another buffer              */
     CC3D_ERR_CUDA = 5,            /* a CUDA runtime call failed                     */
     CC3D_ERR_OOM = 6,             /* host allocation failed                         */
@@ -104,7 +106,7 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T_chunk, const void* x_chun
                                void* stream);
 
 /* Zero a cache buffer ([kt-1][H][W][Cin]) on the stream: the history of a new
- * video.  Stream-ordered, no allocation.  Same alignment rule as the tensors. */
+ * video.  Stream-ordered, no allocation.  Same alignment rule as cache_out. */
 cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream);
 
 /* Synchronise the stream, then report (and clear) the device status word and

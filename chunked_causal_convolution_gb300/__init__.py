@@ -27,7 +27,8 @@ __all__ = [
     "CC3D_F32", "CC3D_BF16", "CC3DError", "CausalConv3dPlan",
     "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_reset", "cc3d_get_status", "cc3d_destroy",
     "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
-    "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "library_path", "load_library",
+    "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_last_error_detail", "library_path",
+    "load_library",
     "weights_from_torch_layout", "EXPORTED_SYMBOLS",
 ]
 
@@ -43,7 +44,7 @@ STATUS_NAMES = {
 EXPORTED_SYMBOLS = (
     "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_reset", "cc3d_get_status", "cc3d_destroy",
     "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
-    "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault",
+    "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_last_error_detail",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -56,6 +57,8 @@ class CC3DError(RuntimeError):
         self.code = code
         self.name = STATUS_NAMES.get(code, str(code))
         msg = "%s (%s)" % (self.name, _status_text(code))
+        if code == 5:
+            msg += ": " + cc3d_last_error_detail()
         super().__init__("%s: %s" % (what, msg) if what else msg)
 
 
@@ -88,6 +91,8 @@ def load_library():
         lib.cc3d_plan_launches_per_chunk.argtypes = [vp]
         lib.cc3d_debug_set_wait_budget_ns.argtypes = [vp, u64]
         lib.cc3d_debug_set_fault.argtypes = [vp, i]
+        lib.cc3d_last_error_detail.argtypes = []
+        lib.cc3d_last_error_detail.restype = ctypes.c_char_p
         for f in (lib.cc3d_plan_create, lib.cc3d_forward_chunk, lib.cc3d_reset, lib.cc3d_get_status,
                   lib.cc3d_plan_launches_per_chunk, lib.cc3d_debug_set_wait_budget_ns,
                   lib.cc3d_debug_set_fault):
@@ -167,6 +172,10 @@ def cc3d_get_status(plan, stream=None) -> int:
 def cc3d_destroy(plan):
     if plan:
         load_library().cc3d_destroy(plan)
+
+
+def cc3d_last_error_detail() -> str:
+    return load_library().cc3d_last_error_detail().decode()
 
 
 def cc3d_status_string(code: int) -> str:

@@ -9,7 +9,7 @@
 #include <mutex>
 #include <new>
 
-#include "../../include/cc3d.h"
+#include "cc3d.h"
 #include "cc3d_internal.h"
 
 namespace cc3d {
@@ -31,13 +31,22 @@ struct DeviceInfo {
 };
 
 std::mutex g_mutex;
+thread_local const char* g_last_detail = "none";
+
+// Record what failed (for cc3d_last_error_detail) and return CC3D_ERR_CUDA.
+cc3d_status cuda_fail(const char* what, cudaError_t e = cudaSuccess)
+{
+    g_last_detail = (e != cudaSuccess) ? cudaGetErrorName(e) : what;
+    return CC3D_ERR_CUDA;
+}
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 cc3d_status device_info(DeviceInfo** out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CC3D_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cuda_fail("cudaGetDevice", e);
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceInfo& d = g_dev[dev];
     if (!d.ready) {
@@ -45,16 +54,17 @@ cc3d_status device_info(DeviceInfo** out)
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return CC3D_ERR_CUDA;
+            return cuda_fail("cudaDeviceGetAttribute", cudaGetLastError());
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return CC3D_ERR_CUDA;
+        e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
         if (g_encode == nullptr) {
             cudaDriverEntryPointQueryResult q;
             void* fn = nullptr;
             if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
                     cudaSuccess ||
                 fn == nullptr)
-                return CC3D_ERR_CUDA;
+                return cuda_fail("cuTensorMapEncodeTiled entry point unavailable");
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
         d.sm103 = (major == 10 && minor == 3);
@@ -160,6 +170,8 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
 
 void cc3d_destroy(cc3d_plan_t plan) { delete plan; }
 
+const char* cc3d_last_error_detail(void) { return g_last_detail; }
+
 const char* cc3d_plan_kernel(cc3d_plan_t plan)
 {
     if (plan == nullptr) return nullptr;
@@ -203,8 +215,8 @@ cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream)
     cc3d_status st = device_info(&d);
     if (st != CC3D_OK) return st;
     if (!d->sm103) return CC3D_ERR_UNSUPPORTED;
-    return zero_fill_launch(cache, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CC3D_OK
-                                                                                            : CC3D_ERR_CUDA;
+    const cudaError_t e = zero_fill_launch(cache, bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CC3D_OK : cuda_fail("zero fill launch", e);
 }
 
 cc3d_status cc3d_get_status(cc3d_plan_t plan, void* stream)
@@ -213,12 +225,15 @@ cc3d_status cc3d_get_status(cc3d_plan_t plan, void* stream)
     DeviceInfo* d = nullptr;
     cc3d_status st = device_info(&d);
     if (st != CC3D_OK) return st;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CC3D_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
     unsigned word = 0;
-    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return CC3D_ERR_CUDA;
+    e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word));
+    if (e != cudaSuccess) return cuda_fail("read status word", e);
     if (word != 0) {
         const unsigned zero = 0;
-        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return CC3D_ERR_CUDA;
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_fail("clear status word", e);
         return CC3D_ERR_DEVICE_TIMEOUT;
     }
     return CC3D_OK;
@@ -280,9 +295,8 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     if (T == 0) {
         // only the history moves: cache_out = last P frames of cache_in (or zeros)
         if (P == 0) return CC3D_OK;
-        return cache_update_launch(nullptr, cache_in, cache_out, 0, P, frame_in, stream) == cudaSuccess
-                   ? CC3D_OK
-                   : CC3D_ERR_CUDA;
+        const cudaError_t e = cache_update_launch(nullptr, cache_in, cache_out, 0, P, frame_in, stream);
+        return e == cudaSuccess ? CC3D_OK : cuda_fail("cache update launch", e);
     }
 
     if (p.kind == K_SIMT_F32) {
@@ -301,9 +315,10 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
         L.bias = static_cast<const float*>(b);
         L.res = static_cast<const float*>(res);
         L.y = static_cast<float*>(y);
-        if (simt_f32_launch(L, stream) != cudaSuccess) return CC3D_ERR_CUDA;
-        if (P > 0 && cache_update_launch(x, cache_in, cache_out, T, P, frame_in, stream) != cudaSuccess)
-            return CC3D_ERR_CUDA;
+        cudaError_t e = simt_f32_launch(L, stream);
+        if (e != cudaSuccess) return cuda_fail("fp32 kernel launch", e);
+        if (P > 0 && (e = cache_update_launch(x, cache_in, cache_out, T, P, frame_in, stream)) != cudaSuccess)
+            return cuda_fail("cache update launch", e);
         return CC3D_OK;
     }
 
@@ -311,7 +326,7 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     TcLaunch L;
     memset(&L, 0, sizeof(L));
     if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, &L)) return CC3D_ERR_UNSUPPORTED;
-    if (p.fault == 2) return CC3D_ERR_CUDA;  // injected host-side encode failure: nothing launched
+    if (p.fault == 2) return cuda_fail("injected tensor-map encode failure");  // nothing launched
     const CUtensorMapSwizzle sw = p.CB == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : p.CB == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                : CU_TENSOR_MAP_SWIZZLE_32B;
@@ -324,24 +339,24 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
         if (g_encode(&L.map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return CC3D_ERR_CUDA;
+            return cuda_fail("cuTensorMapEncodeTiled (x_chunk)");
         if (cache_in != nullptr) {
             const cuuint64_t cdims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)P};
             if (g_encode(&L.map_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache_in), cdims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-                return CC3D_ERR_CUDA;
+                return cuda_fail("cuTensorMapEncodeTiled (cache_in)");
         }
     }
     {
-        // weights [Cout][27][Cin] seen as (ci, co, tap) so one box holds `taps_b` K-major tap tiles
+        // weights [Cout][27][Cin] seen as (ci, co, tap) so one box holds three K-major tap tiles
         const cuuint64_t dims[3] = {(cuuint64_t)p.Cin, (cuuint64_t)p.Cout, 27};
         const cuuint64_t strides[2] = {(cuuint64_t)27 * p.Cin * 2, (cuuint64_t)p.Cin * 2};
-        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)L.NT, (cuuint32_t)L.taps_b};
+        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)L.NT, 3};
         if (g_encode(&L.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return CC3D_ERR_CUDA;
+            return cuda_fail("cuTensorMapEncodeTiled (w)");
     }
     L.has_cache = cache_in != nullptr;
     L.bias = b;
@@ -355,7 +370,8 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     L.fault = p.fault;
     const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * T;
     L.grid = ntiles < d->sms ? ntiles : d->sms;
-    return tc_launch(p.CB, L, stream) == cudaSuccess ? CC3D_OK : CC3D_ERR_CUDA;
+    const cudaError_t e = tc_launch(p.CB, L, stream);
+    return e == cudaSuccess ? CC3D_OK : cuda_fail("tensor-core kernel launch", e);
 }
 
 }  // extern "C"

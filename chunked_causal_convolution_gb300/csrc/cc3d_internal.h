@@ -39,9 +39,9 @@ struct TcLaunch {
     // tensor maps (encoded on the host)
     CUtensorMap map_x;      // x_chunk   [T][H][W][Cin]   box (CB, Sp, nrows, 1)
     CUtensorMap map_cache;  // cache_in  [P][H][W][Cin]   same box (unused if no cache)
-    CUtensorMap map_w;      // w viewed as (Cin, Cout, taps) box (CB, NT, taps_b)
+    CUtensorMap map_w;      // w viewed as (Cin, Cout, taps) box (CB, NT, 3)
     int T, H, W, Cin, Cout;
-    int NT, nsplit, acc_stages, taps_b;
+    int NT, nsplit, acc_stages;
     int na, nb;                       // A / B ring stages
     int a_stage_bytes, b_stage_bytes;
     int tmem_cols;                    // allocated columns (power of two)

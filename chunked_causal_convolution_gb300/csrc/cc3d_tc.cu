@@ -15,12 +15,18 @@
 //     spatial zero padding.  Frames before the chunk come from the caller's
 //     cache (or read as zeros through a negative frame coordinate when there is
 //     no cache), which is the causal history.
-//   * B: the weights of `taps_b` taps for the same channel block, K-major.
+//   * B: one stage = the weights of the three taps of one (dt, dh) row for one
+//     channel block and one N slice, K-major.
 //
 // Warp roles (256 threads): warp 0 = TMA loader, warp 1 = MMA issuer, warp 2
 // = tensor-memory allocator and, with warp 3, the copy of the new temporal
 // cache, warps 4-7 = epilogue (tensor memory -> registers -> + bias
 // [+ residual] -> bf16 -> global), one output position per thread.
+//
+// The MMA issuer keeps the shared-memory descriptors of stage 0 and advances
+// them by additions only (the start-address field is the low 14 bits and every
+// address stays below 2^18 bytes), with the tap / row-group / K-step loops
+// unrolled at compile time.
 //
 // The accumulation order of every output is fixed: dt, channel block, dh, dw,
 // 16-channel step -- it depends neither on the tile an output falls in nor on
@@ -39,7 +45,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxStages = 8;
 constexpr int kMaxAcc = 2;
-constexpr int kMaxSub = 4;
 
 struct TileCoord {
     int t, w0, f0, hstart;
@@ -76,10 +81,56 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return (uint32_t)__bfloat16_as_ushort(l) | ((uint32_t)__bfloat16_as_ushort(h) << 16);
 }
 
-template <int CB>
+// 16 accumulator columns of one output position: + bias (+ residual) -> bf16 -> global.
+__device__ __forceinline__ void store16(const uint32_t* r, const float* s_bias, int co0, size_t px, int Cout,
+                                        bool wide, const __nv_bfloat16* res, __nv_bfloat16* y)
+{
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = __fadd_rn(__uint_as_float(r[k]), s_bias[co0 + k]);
+    if (wide) {
+        const size_t off = px * Cout + co0;
+        if (res != nullptr) {
+            const uint4 r0 = __ldg(reinterpret_cast<const uint4*>(res + off));
+            const uint4 r1 = __ldg(reinterpret_cast<const uint4*>(res + off + 8));
+            const uint32_t rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                v[2 * k] = __fadd_rn(v[2 * k], bf16_lo(rr[k]));
+                v[2 * k + 1] = __fadd_rn(v[2 * k + 1], bf16_hi(rr[k]));
+            }
+        }
+        uint4 o0, o1;
+        o0.x = pack_bf16x2(v[0], v[1]);
+        o0.y = pack_bf16x2(v[2], v[3]);
+        o0.z = pack_bf16x2(v[4], v[5]);
+        o0.w = pack_bf16x2(v[6], v[7]);
+        o1.x = pack_bf16x2(v[8], v[9]);
+        o1.y = pack_bf16x2(v[10], v[11]);
+        o1.z = pack_bf16x2(v[12], v[13]);
+        o1.w = pack_bf16x2(v[14], v[15]);
+        *reinterpret_cast<uint4*>(y + off) = o0;
+        *reinterpret_cast<uint4*>(y + off + 8) = o1;
+    } else {
+        // narrow output head: fewer than 16 channels, element stores
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int co = co0 + k;
+            if (co < Cout) {
+                const size_t off = px * Cout + co;
+                float o = v[k];
+                if (res != nullptr) o = __fadd_rn(o, __bfloat162float(res[off]));
+                y[off] = __float2bfloat16_rn(o);
+            }
+        }
+    }
+}
+
+template <int CB, int SUB>
 __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_constant__ TcLaunch L)
 {
-    constexpr uint32_t ROWB = CB * 2;  // bytes of one pixel row of a channel block = swizzle span
+    constexpr uint32_t ROWB = CB * 2;     // bytes of one pixel row of a channel block = swizzle span
+    constexpr uint32_t ROWU = ROWB / 16;  // the same in descriptor address units
     constexpr uint32_t LAYOUT = CB == 64 ? LAYOUT_SW128 : (CB == 32 ? LAYOUT_SW64 : LAYOUT_SW32);
     constexpr uint32_t SBO = 8 * ROWB;
     constexpr int KSTEPS = CB / 16;
@@ -99,12 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
     const int Sp = L.g.Sp;
     const int NT = L.NT;
     const int nsplit = L.nsplit;
-    const int sub = L.g.sub;
     const int ncb = L.Cin / CB;
-    const int bper = 9 / L.taps_b;  // B stages per (dt, cb)
     const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * L.T;
     const int cout_pad = nsplit * NT;
-    const uint32_t acc_cols = (uint32_t)(sub * nsplit * NT);
+    const uint32_t acc_cols = (uint32_t)(SUB * nsplit * NT);
     const unsigned long long budget = L.wait_ns;
 
     if (threadIdx.x == 0) {
@@ -141,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             int last_pa[kMaxStages], last_pb[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) last_pa[s] = last_pb[s] = -1;
             const uint32_t a_tx = (uint32_t)(ROWB * Sp * L.g.nrows);
-            const uint32_t b_tx = (uint32_t)(ROWB * NT * L.taps_b * nsplit);
+            const uint32_t b_tx = (uint32_t)(ROWB * NT * 3);
             bool skip_first = (L.fault == 1);
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
@@ -164,20 +213,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                         skip_first = false;
                         last_pa[sa] = pa;
                         if (++sa == L.na) { sa = 0; pa ^= 1; }
-                        for (int tb = 0; tb < bper; ++tb) {
-                            if (!bounded_wait(&b_empty[sb], pb ^ 1, budget, &abort_flag)) {
-                                if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
-                                ok = false;
-                                break;
+                        for (int dh = 0; ok && dh < 3; ++dh) {
+                            for (int ns = 0; ns < nsplit; ++ns) {
+                                if (!bounded_wait(&b_empty[sb], pb ^ 1, budget, &abort_flag)) {
+                                    if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
+                                    ok = false;
+                                    break;
+                                }
+                                mbar_arrive_expect_tx(&b_full[sb], b_tx);
+                                tma_load_3d(smB + (size_t)sb * L.b_stage_bytes, &L.map_w, &b_full[sb], cb * CB,
+                                            ns * NT, dt * 9 + dh * 3);
+                                last_pb[sb] = pb;
+                                if (++sb == L.nb) { sb = 0; pb ^= 1; }
                             }
-                            mbar_arrive_expect_tx(&b_full[sb], b_tx);
-                            const int tap0 = dt * 9 + tb * L.taps_b;
-                            uint8_t* dst = smB + (size_t)sb * L.b_stage_bytes;
-                            for (int ns = 0; ns < nsplit; ++ns)
-                                tma_load_3d(dst + (size_t)ns * L.taps_b * NT * ROWB, &L.map_w, &b_full[sb], cb * CB,
-                                            ns * NT, tap0);
-                            last_pb[sb] = pb;
-                            if (++sb == L.nb) { sb = 0; pb ^= 1; }
                         }
                     }
                 }
@@ -194,6 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = make_idesc_bf16_f32(128, NT);
+            const uint64_t a_desc0 = make_sdesc(smem_u32(smA), 16, SBO, LAYOUT, 0);
+            const uint64_t b_desc0 = make_sdesc(smem_u32(smB), 16, SBO, LAYOUT, 0);
+            const uint32_t a_inc = (uint32_t)L.a_stage_bytes >> 4;
+            const uint32_t b_inc = (uint32_t)L.b_stage_bytes >> 4;
+            const uint32_t b_tap_inc = (uint32_t)NT * ROWU;  // next tap inside a B stage
+            const uint32_t row_shift = (uint32_t)Sp * ROWU;  // next padded row inside the A window
             int sa = 0, pa = 0, sb = 0, pb = 0;
             bool ok = true;
             int it = 0;
@@ -207,8 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                 }
                 tc_fence_after();
                 const uint32_t dbase = tmem + (uint32_t)as * acc_cols;
-                int rowoff[kMaxSub];
-                for (int m = 0; m < kMaxSub; ++m) rowoff[m] = c.f0 + m * L.g.sub_stride - c.hstart * Sp - Sp - 1;
+                // window row of the (dh = 0, dw = 0) view of each 128-row group, in descriptor units
+                uint32_t rowu[SUB];
+#pragma unroll
+                for (int m = 0; m < SUB; ++m)
+                    rowu[m] = (uint32_t)(c.f0 + m * L.g.sub_stride - c.hstart * Sp - Sp - 1) * ROWU;
                 for (int dt = 0; ok && dt < 3; ++dt) {
                     for (int cb = 0; ok && cb < ncb; ++cb) {
                         if (!bounded_wait(&a_full[sa], pa, budget, &abort_flag)) {
@@ -217,37 +274,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t abase = smem_u32(smA + (size_t)sa * L.a_stage_bytes);
-                        for (int tb = 0; tb < bper; ++tb) {
-                            if (!bounded_wait(&b_full[sb], pb, budget, &abort_flag)) {
-                                if (!abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t bbase = smem_u32(smB + (size_t)sb * L.b_stage_bytes);
-                            for (int j = 0; j < L.taps_b; ++j) {
-                                const int tap = tb * L.taps_b + j;
-                                const int dh = tap / 3, dw = tap - 3 * (tap / 3);
-                                const int shift = dh * Sp + dw;
-                                for (int m = 0; m < sub; ++m) {
-                                    const uint32_t arow = abase + (uint32_t)(rowoff[m] + shift) * ROWB;
+                        const uint64_t a_st = a_desc0 + (uint64_t)(sa * a_inc);
+                        for (int dh = 0; ok && dh < 3; ++dh) {
+                            const uint64_t a_row = a_st + (uint64_t)(dh * row_shift);
+                            const bool first_row = (dt | cb | dh) == 0;
+                            for (int ns = 0; ns < nsplit; ++ns) {
+                                if (!bounded_wait(&b_full[sb], pb, budget, &abort_flag)) {
+                                    if (!abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                const uint64_t b_st = b_desc0 + (uint64_t)(sb * b_inc);
+                                const uint32_t dcol = dbase + (uint32_t)(ns * NT);
 #pragma unroll
-                                    for (int ks = 0; ks < KSTEPS; ++ks) {
-                                        const uint64_t ad = make_sdesc(arow + ks * 32, 16, SBO, LAYOUT, 0);
-                                        const uint32_t acc = (dt | cb | tap | ks) != 0;
-                                        for (int ns = 0; ns < nsplit; ++ns) {
-                                            const uint64_t bd = make_sdesc(
-                                                bbase + (uint32_t)((ns * L.taps_b + j) * NT) * ROWB + ks * 32, 16,
-                                                SBO, LAYOUT, 0);
-                                            umma_bf16_ss(dbase + (uint32_t)((m * nsplit + ns) * NT), ad, bd, idesc,
-                                                         acc);
+                                for (int dw = 0; dw < 3; ++dw) {
+#pragma unroll
+                                    for (int m = 0; m < SUB; ++m) {
+#pragma unroll
+                                        for (int ks = 0; ks < KSTEPS; ++ks) {
+                                            const uint64_t ad = a_row + (uint64_t)(rowu[m] + dw * ROWU + ks * 2);
+                                            const uint64_t bd = b_st + (uint64_t)(dw * b_tap_inc + ks * 2);
+                                            const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
+                                            umma_bf16_ss(dcol + (uint32_t)(m * nsplit * NT), ad, bd, idesc, acc);
                                         }
                                     }
                                 }
+                                umma_commit(&b_empty[sb]);
+                                if (++sb == L.nb) { sb = 0; pb ^= 1; }
                             }
-                            umma_commit(&b_empty[sb]);
-                            if (++sb == L.nb) { sb = 0; pb ^= 1; }
                         }
                         if (!ok) break;
                         umma_commit(&a_empty[sa]);
@@ -303,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             if (!ready) break;
             tc_fence_after();
             const TileCoord c = tile_coord(L, tile);
-            for (int m = 0; m < sub; ++m) {
+#pragma unroll
+            for (int m = 0; m < SUB; ++m) {
                 const int f = c.f0 + m * L.g.sub_stride + q * 32 + lane;
                 const int h = f / Sp;
                 const int jcol = f - h * Sp;
@@ -311,51 +367,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                 const bool valid = h < L.H && jcol >= 1 && jcol <= L.g.S && w < L.W;
                 const size_t px = ((size_t)c.t * L.H + (valid ? h : 0)) * L.W + (valid ? w : 0);
                 for (int ns = 0; ns < nsplit; ++ns) {
-                    for (int cc = 0; cc < NT; cc += 16) {
-                        uint32_t r[16];
-                        tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
-                                               (uint32_t)((m * nsplit + ns) * NT + cc),
-                                           r);
+                    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
+                                           (uint32_t)((m * nsplit + ns) * NT);
+                    int cc = 0;
+                    for (; cc + 32 <= NT; cc += 32) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tbase + (uint32_t)cc, r);
                         tmem_ld_wait();
-                        if (!valid) continue;
-                        const int co0 = ns * NT + cc;
-                        float v[16];
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) v[k] = __fadd_rn(__uint_as_float(r[k]), s_bias[co0 + k]);
-                        if (wide) {
-                            const size_t off = px * L.Cout + co0;
-                            if (res != nullptr) {
-                                const uint4 r0 = __ldg(reinterpret_cast<const uint4*>(res + off));
-                                const uint4 r1 = __ldg(reinterpret_cast<const uint4*>(res + off + 8));
-                                const uint32_t rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-                                for (int k = 0; k < 8; ++k) {
-                                    v[2 * k] = __fadd_rn(v[2 * k], bf16_lo(rr[k]));
-                                    v[2 * k + 1] = __fadd_rn(v[2 * k + 1], bf16_hi(rr[k]));
-                                }
-                            }
-                            uint4 o0, o1;
-                            o0.x = pack_bf16x2(v[0], v[1]);
-                            o0.y = pack_bf16x2(v[2], v[3]);
-                            o0.z = pack_bf16x2(v[4], v[5]);
-                            o0.w = pack_bf16x2(v[6], v[7]);
-                            o1.x = pack_bf16x2(v[8], v[9]);
-                            o1.y = pack_bf16x2(v[10], v[11]);
-                            o1.z = pack_bf16x2(v[12], v[13]);
-                            o1.w = pack_bf16x2(v[14], v[15]);
-                            *reinterpret_cast<uint4*>(y + off) = o0;
-                            *reinterpret_cast<uint4*>(y + off + 8) = o1;
-                        } else {
-                            // narrow output head: fewer than 16 channels, element stores
-                            for (int k = 0; k < 16; ++k) {
-                                const int co = co0 + k;
-                                if (co >= L.Cout) break;
-                                const size_t off = px * L.Cout + co;
-                                float o = v[k];
-                                if (res != nullptr) o = __fadd_rn(o, __bfloat162float(res[off]));
-                                y[off] = __float2bfloat16_rn(o);
-                            }
+                        if (valid) {
+                            store16(r, s_bias, ns * NT + cc, px, L.Cout, wide, res, y);
+                            store16(r + 16, s_bias, ns * NT + cc + 16, px, L.Cout, wide, res, y);
                         }
+                    }
+                    if (cc < NT) {  // NT % 32 == 16
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(tbase + (uint32_t)cc, r);
+                        tmem_ld_wait();
+                        if (valid) store16(r, s_bias, ns * NT + cc, px, L.Cout, wide, res, y);
                     }
                 }
             }
@@ -379,18 +407,29 @@ int env_int(const char* name, int dflt)
     return (s != nullptr && *s) ? atoi(s) : dflt;
 }
 
+template <int CB>
+void* kernel_for_sub(int sub)
+{
+    switch (sub) {
+    case 1: return reinterpret_cast<void*>(tc_bf16_kernel<CB, 1>);
+    case 2: return reinterpret_cast<void*>(tc_bf16_kernel<CB, 2>);
+    case 4: return reinterpret_cast<void*>(tc_bf16_kernel<CB, 4>);
+    default: return nullptr;
+    }
+}
+
 }  // namespace
 
 bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
 {
-    if (CB != 16 && CB != 32 && CB != 64) return false;
+    if (CB != 16 && CB != 32) return false;
     if (Cin % CB != 0) return false;
     L->T = T;
     L->H = H;
     L->W = W;
     L->Cin = Cin;
     L->Cout = Cout;
-    // output channels per MMA (N) and number of N splits
+    // output channels per MMA (N) and number of N slices
     if (Cout < 16) {
         L->NT = 16;
         L->nsplit = 1;
@@ -403,17 +442,17 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
         L->NT = Cout / ns;
     }
     const int ntot = L->NT * L->nsplit;
-    // tensor-memory budget: sub * ntot * acc_stages <= 512 columns
+    // tensor-memory budget: sub * ntot * acc_stages <= 512 columns, sub in {1, 2, 4}
     int sub = 256 / ntot, acc = 2;
     if (sub < 1) {
         acc = 1;
         sub = 512 / ntot;
         if (sub < 1) return false;
     }
-    if (sub > kMaxSub) sub = kMaxSub;
+    sub = sub >= 4 ? 4 : (sub >= 2 ? 2 : 1);
     sub = env_int("CC3D_TC_SUB", sub);
     acc = env_int("CC3D_TC_ACC", acc);
-    if (sub < 1 || sub > kMaxSub || acc < 1 || acc > kMaxAcc || sub * ntot * acc > 512) return false;
+    if ((sub != 1 && sub != 2 && sub != 4) || acc < 1 || acc > kMaxAcc || sub * ntot * acc > 512) return false;
     L->acc_stages = acc;
     int cols = 32;
     while (cols < sub * ntot * acc) cols *= 2;
@@ -448,8 +487,7 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
     const int rowb = CB * 2;
     const int a_bytes = rowb * g.Sp * g.nrows;
     L->a_stage_bytes = (a_bytes + 1023) & ~1023;
-    L->taps_b = (3 * ntot * rowb <= 40 * 1024) ? 3 : 1;
-    L->b_stage_bytes = (L->taps_b * ntot * rowb + 1023) & ~1023;
+    L->b_stage_bytes = (3 * L->NT * rowb + 1023) & ~1023;
     const int budget = 220 * 1024 - 4 * ntot;
     L->na = (L->a_stage_bytes > 40 * 1024) ? 2 : 3;
     L->na = env_int("CC3D_TC_NA", L->na);
@@ -471,17 +509,12 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
 
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream)
 {
-    void (*kern)(TcLaunch) = nullptr;
-    if (CB == 16)
-        kern = tc_bf16_kernel<16>;
-    else if (CB == 32)
-        kern = tc_bf16_kernel<32>;
-    else
-        kern = tc_bf16_kernel<64>;
+    void* kern = CB == 16 ? kernel_for_sub<16>(L.g.sub) : kernel_for_sub<32>(L.g.sub);
+    if (kern == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<L.grid, kThreads, L.smem_bytes, stream>>>(L);
-    return cudaGetLastError();
+    void* args[] = {const_cast<TcLaunch*>(&L)};
+    return cudaLaunchKernel(kern, dim3(L.grid), dim3(kThreads), args, L.smem_bytes, stream);
 }
 
 }  // namespace cc3d

@@ -116,6 +116,10 @@ cc3d_status cc3d_get_status(cc3d_plan_t plan, void* stream);
 /* Release the plan (NULL is accepted). */
 void cc3d_destroy(cc3d_plan_t plan);
 
+/* Text naming the CUDA call (or CUDA error) behind the last CC3D_ERR_CUDA
+ * returned on the calling thread; "none" before any.  Static storage. */
+const char* cc3d_last_error_detail(void);
+
 /* Static, human-readable text of a status code. */
 const char* cc3d_status_string(cc3d_status s);
 

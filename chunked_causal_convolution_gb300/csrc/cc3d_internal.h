@@ -43,6 +43,7 @@ struct TcLaunch {
     int T, H, W, Cin, Cout;
     int NT, nsplit, acc_stages;
     int na, nb;                       // A / B ring stages
+    int prefetch;                     // temporal taps of the next tile warmed in L2 (0..3)
     int a_stage_bytes, b_stage_bytes;
     int tmem_cols;                    // allocated columns (power of two)
     TcGeometry g;

@@ -83,6 +83,31 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, uin
     }
 }
 
+// Bounded wait done by lane 0 with the verdict broadcast to the warp (keeps control flow warp-uniform).
+__device__ __forceinline__ bool warp_bounded_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns,
+                                                  const volatile int* abort)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = bounded_wait(bar, parity, budget_ns, abort) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// true in exactly one lane of the (fully active) warp
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n"
+        "  .reg .b32 rx;\n"
+        "  .reg .pred px;\n"
+        "  elect.sync rx|px, %1;\n"
+        "  @px mov.s32 %0, 1;\n"
+        "}\n"
+        : "+r"(pred)
+        : "r"(0xffffffffu));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1)
 {
@@ -121,6 +146,14 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, u
         " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
         "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
+}
+
+// warm L2 with a tensor tile (no shared-memory destination, no completion tracking)
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map), "r"(c0),
+                 "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
 }
 
 // shared -> global tiled store (completion tracked by bulk groups)

@@ -23,10 +23,12 @@
 // cache, warps 4-7 = epilogue (tensor memory -> registers -> + bias
 // [+ residual] -> bf16 -> global), one output position per thread.
 //
-// The MMA issuer keeps the shared-memory descriptors of stage 0 and advances
+// The MMA warp keeps the shared-memory descriptors of stage 0 and advances
 // them by additions only (the start-address field is the low 14 bits and every
 // address stays below 2^18 bytes), with the tap / row-group / K-step loops
-// unrolled at compile time.
+// unrolled at compile time.  All 32 lanes walk the issue loop, so the
+// descriptors stay warp-uniform, and an elected lane issues each MMA: issuing
+// from a single divergent lane instead costs about 1.6x the time per MMA.
 //
 // The accumulation order of every output is fixed: dt, channel block, dh, dw,
 // 16-channel step -- it depends neither on the tile an output falls in nor on
@@ -195,6 +197,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
                 const TileCoord c = tile_coord(L, tile);
+                // optionally warm L2 with the input windows of this block's next tile
+                const int next = tile + (int)gridDim.x;
+                if (L.prefetch && next < ntiles) {
+                    const TileCoord n = tile_coord(L, next);
+                    for (int dt = 3 - L.prefetch; dt < 3; ++dt) {
+                        const int tin = n.t + dt - 2;
+                        const bool from_cache = tin < 0 && L.has_cache;
+                        for (int cb = 0; cb < ncb; ++cb)
+                            tma_prefetch_4d(from_cache ? &L.map_cache : &L.map_x, cb * CB, n.w0 - 1, n.hstart,
+                                            from_cache ? tin + 2 : tin);
+                    }
+                }
                 for (int dt = 0; ok && dt < 3; ++dt) {
                     const int tin = c.t + dt - 2;
                     const CUtensorMap* map = &L.map_x;
@@ -240,82 +254,84 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = make_idesc_bf16_f32(128, NT);
-            const uint64_t a_desc0 = make_sdesc(smem_u32(smA), 16, SBO, LAYOUT, 0);
-            const uint64_t b_desc0 = make_sdesc(smem_u32(smB), 16, SBO, LAYOUT, 0);
-            const uint32_t a_inc = (uint32_t)L.a_stage_bytes >> 4;
-            const uint32_t b_inc = (uint32_t)L.b_stage_bytes >> 4;
-            const uint32_t b_tap_inc = (uint32_t)NT * ROWU;  // next tap inside a B stage
-            const uint32_t row_shift = (uint32_t)Sp * ROWU;  // next padded row inside the A window
-            int sa = 0, pa = 0, sb = 0, pb = 0;
-            bool ok = true;
-            int it = 0;
-            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
-                const TileCoord c = tile_coord(L, tile);
-                const int as = it % L.acc_stages;
-                const int aph = (it / L.acc_stages) & 1;
-                if (!bounded_wait(&acc_empty[as], aph ^ 1, budget, &abort_flag)) {
-                    if (!abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t dbase = tmem + (uint32_t)as * acc_cols;
-                // window row of the (dh = 0, dw = 0) view of each 128-row group, in descriptor units
-                uint32_t rowu[SUB];
+        // The whole warp walks the loop so that every descriptor stays warp-uniform (the MMA takes
+        // its operands from uniform registers); one elected lane issues each tcgen05 instruction.
+        const uint32_t idesc = make_idesc_bf16_f32(128, NT);
+        const uint64_t a_desc0 = make_sdesc(smem_u32(smA), 16, SBO, LAYOUT, 0);
+        const uint64_t b_desc0 = make_sdesc(smem_u32(smB), 16, SBO, LAYOUT, 0);
+        const uint32_t a_inc = (uint32_t)L.a_stage_bytes >> 4;
+        const uint32_t b_inc = (uint32_t)L.b_stage_bytes >> 4;
+        const uint32_t b_tap_inc = (uint32_t)NT * ROWU;  // next tap inside a B stage
+        const uint32_t row_shift = (uint32_t)Sp * ROWU;  // next padded row inside the A window
+        const uint32_t m_cols = (uint32_t)(nsplit * NT);  // tensor-memory columns per row group
+        int sa = 0, pa = 0, sb = 0, pb = 0;
+        bool ok = true;
+        int it = 0;
+        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+            const TileCoord c = tile_coord(L, tile);
+            const int as = it % L.acc_stages;
+            const int aph = (it / L.acc_stages) & 1;
+            if (!warp_bounded_wait(&acc_empty[as], aph ^ 1, budget, &abort_flag)) {
+                if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t dbase = tmem + (uint32_t)as * acc_cols;
+            // window row of the (dh = 0, dw = 0) view of each 128-row group, in descriptor units
+            uint32_t rowu[SUB];
 #pragma unroll
-                for (int m = 0; m < SUB; ++m)
-                    rowu[m] = (uint32_t)(c.f0 + m * L.g.sub_stride - c.hstart * Sp - Sp - 1) * ROWU;
-                for (int dt = 0; ok && dt < 3; ++dt) {
-                    for (int cb = 0; ok && cb < ncb; ++cb) {
-                        if (!bounded_wait(&a_full[sa], pa, budget, &abort_flag)) {
-                            if (!abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t a_st = a_desc0 + (uint64_t)(sa * a_inc);
-                        for (int dh = 0; ok && dh < 3; ++dh) {
-                            const uint64_t a_row = a_st + (uint64_t)(dh * row_shift);
-                            const bool first_row = (dt | cb | dh) == 0;
-                            for (int ns = 0; ns < nsplit; ++ns) {
-                                if (!bounded_wait(&b_full[sb], pb, budget, &abort_flag)) {
-                                    if (!abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                                const uint64_t b_st = b_desc0 + (uint64_t)(sb * b_inc);
-                                const uint32_t dcol = dbase + (uint32_t)(ns * NT);
+            for (int m = 0; m < SUB; ++m)
+                rowu[m] = (uint32_t)(c.f0 + m * L.g.sub_stride - c.hstart * Sp - Sp - 1) * ROWU;
+            for (int dt = 0; ok && dt < 3; ++dt) {
+                for (int cb = 0; ok && cb < ncb; ++cb) {
+                    if (!warp_bounded_wait(&a_full[sa], pa, budget, &abort_flag)) {
+                        if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a_st = a_desc0 + (uint64_t)(sa * a_inc);
+                    for (int dh = 0; ok && dh < 3; ++dh) {
+                        const uint64_t a_row = a_st + (uint64_t)(dh * row_shift);
+                        const bool first_row = (dt | cb | dh) == 0;
+                        for (int ns = 0; ns < nsplit; ++ns) {
+                            if (!warp_bounded_wait(&b_full[sb], pb, budget, &abort_flag)) {
+                                if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint64_t b_st = b_desc0 + (uint64_t)(sb * b_inc);
+                            const uint32_t dcol = dbase + (uint32_t)(ns * NT);
 #pragma unroll
-                                for (int dw = 0; dw < 3; ++dw) {
+                            for (int dw = 0; dw < 3; ++dw) {
 #pragma unroll
-                                    for (int m = 0; m < SUB; ++m) {
+                                for (int m = 0; m < SUB; ++m) {
 #pragma unroll
-                                        for (int ks = 0; ks < KSTEPS; ++ks) {
-                                            const uint64_t ad = a_row + (uint64_t)(rowu[m] + dw * ROWU + ks * 2);
-                                            const uint64_t bd = b_st + (uint64_t)(dw * b_tap_inc + ks * 2);
-                                            const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
-                                            umma_bf16_ss(dcol + (uint32_t)(m * nsplit * NT), ad, bd, idesc, acc);
-                                        }
+                                    for (int ks = 0; ks < KSTEPS; ++ks) {
+                                        const uint64_t ad = a_row + (uint64_t)(rowu[m] + dw * ROWU + ks * 2);
+                                        const uint64_t bd = b_st + (uint64_t)(dw * b_tap_inc + ks * 2);
+                                        const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
+                                        if (elect_one()) umma_bf16_ss(dcol + (uint32_t)m * m_cols, ad, bd, idesc, acc);
                                     }
                                 }
-                                umma_commit(&b_empty[sb]);
-                                if (++sb == L.nb) { sb = 0; pb ^= 1; }
                             }
+                            if (elect_one()) umma_commit(&b_empty[sb]);
+                            if (++sb == L.nb) { sb = 0; pb ^= 1; }
                         }
-                        if (!ok) break;
-                        umma_commit(&a_empty[sa]);
-                        if (++sa == L.na) { sa = 0; pa ^= 1; }
                     }
+                    if (!ok) break;
+                    if (elect_one()) umma_commit(&a_empty[sa]);
+                    if (++sa == L.na) { sa = 0; pa ^= 1; }
                 }
-                if (!ok) break;
-                umma_commit(&acc_full[as]);
             }
-            // wait until every MMA this thread issued has finished writing tensor memory
-            umma_commit(&mma_drain);
-            if (!bounded_wait(&mma_drain, 0, budget, nullptr)) atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
+            if (!ok) break;
+            if (elect_one()) umma_commit(&acc_full[as]);
         }
+        // wait until every MMA this warp issued has finished writing tensor memory
+        if (elect_one()) umma_commit(&mma_drain);
+        __syncwarp();
+        if (!warp_bounded_wait(&mma_drain, 0, budget, nullptr) && lane == 0) atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
     } else if (warp == 2 || warp == 3) {
         // ------------------------------------------------------------ temporal cache update
         // cache_out[j] = frame (T + j) of concat(cache_in, x); j < 2.
@@ -325,18 +341,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         const uint4* xin = reinterpret_cast<const uint4*>(L.x);
         const uint4* cin = reinterpret_cast<const uint4*>(L.cache_in);
         uint4* cout_ = reinterpret_cast<uint4*>(L.cache_out);
-        for (size_t i = (size_t)blockIdx.x * 64 + (threadIdx.x - 64); i < total; i += gthreads) {
-            const int j = (int)(i / frame_chunks);
-            const size_t o = i - (size_t)j * frame_chunks;
-            const int src = L.T + j;  // index in the extended stack
-            uint4 v;
-            if (src >= 2)
-                v = __ldg(xin + (size_t)(src - 2) * frame_chunks + o);
-            else if (cin != nullptr)
-                v = __ldg(cin + (size_t)src * frame_chunks + o);
-            else
-                v = make_uint4(0, 0, 0, 0);
-            cout_[i] = v;
+        // 8 independent 16-byte loads in flight per thread before their stores
+        constexpr int U = 8;
+        for (size_t i0 = ((size_t)blockIdx.x * 64 + (threadIdx.x - 64)) * U; i0 < total; i0 += gthreads * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const size_t i = i0 + u;
+                v[u] = make_uint4(0, 0, 0, 0);
+                if (i < total) {
+                    const int j = (int)(i / frame_chunks);
+                    const size_t o = i - (size_t)j * frame_chunks;
+                    const int src = L.T + j;  // index in the extended stack
+                    if (src >= 2)
+                        v[u] = __ldg(xin + (size_t)(src - 2) * frame_chunks + o);
+                    else if (cin != nullptr)
+                        v[u] = __ldg(cin + (size_t)src * frame_chunks + o);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (i0 + u < total) __stcs(cout_ + i0 + u, v[u]);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -494,6 +519,8 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
     if (L->na < 2 || L->na > kMaxStages) return false;
     int nb = (budget - L->na * L->a_stage_bytes) / L->b_stage_bytes;
     if (nb > kMaxStages) nb = kMaxStages;
+    const int nb_env = env_int("CC3D_TC_NB", 0);
+    if (nb_env >= 2 && nb_env < nb) nb = nb_env;
     if (nb < 2) {
         L->na = 2;
         nb = (budget - L->na * L->a_stage_bytes) / L->b_stage_bytes;
@@ -501,6 +528,10 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
         if (nb < 2) return false;
     }
     L->nb = nb;
+    // L2 prefetch of the next tile's windows: 0 none, 1..3 = that many temporal taps (newest first);
+    // off by default: measured slower on every decoder shape (it competes with the live working set)
+    L->prefetch = env_int("CC3D_TC_PREFETCH", 0);
+    if (L->prefetch < 0 || L->prefetch > 3) L->prefetch = 0;
     L->smem_bytes = (size_t)L->na * L->a_stage_bytes + (size_t)L->nb * L->b_stage_bytes + 4 * ntot + 1024;
     // one block per SM: a second resident block would wait inside its tensor-memory allocation
     if (L->smem_bytes < 120 * 1024) L->smem_bytes = 120 * 1024;

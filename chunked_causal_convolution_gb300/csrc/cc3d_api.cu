@@ -147,7 +147,8 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
         CB = (Cin % 32 == 0) ? 32 : 16;
         TcLaunch probe;
         memset(&probe, 0, sizeof(probe));
-        if (!tc_configure(CB, 1, H, W, Cin, Cout, &probe)) return CC3D_ERR_UNSUPPORTED;
+        if (!tc_configure(CB, 1, H, W, Cin, Cout, false, &probe) || !tc_configure(CB, 1, H, W, Cin, Cout, true, &probe))
+            return CC3D_ERR_UNSUPPORTED;
         kind = Cout < 16 ? K_TC_BF16_NARROW : K_TC_BF16;
     }
     cc3d_plan_s* p = new (std::nothrow) cc3d_plan_s;
@@ -325,7 +326,7 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     // ---- tensor-core path
     TcLaunch L;
     memset(&L, 0, sizeof(L));
-    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, &L)) return CC3D_ERR_UNSUPPORTED;
+    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, res != nullptr, &L)) return CC3D_ERR_UNSUPPORTED;
     if (p.fault == 2) return cuda_fail("injected tensor-map encode failure");  // nothing launched
     const CUtensorMapSwizzle sw = p.CB == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : p.CB == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -349,10 +350,10 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
         }
     }
     {
-        // weights [Cout][27][Cin] seen as (ci, co, tap) so one box holds three K-major tap tiles
+        // weights [Cout][27][Cin] seen as (ci, co, tap) so one box holds 3 * rb K-major tap tiles
         const cuuint64_t dims[3] = {(cuuint64_t)p.Cin, (cuuint64_t)p.Cout, 27};
         const cuuint64_t strides[2] = {(cuuint64_t)27 * p.Cin * 2, (cuuint64_t)p.Cin * 2};
-        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)L.NT, 3};
+        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)L.NT, (cuuint32_t)(3 * L.rb)};
         if (g_encode(&L.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -368,7 +369,7 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     L.status = d->status;
     L.wait_ns = p.wait_ns;
     L.fault = p.fault;
-    const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * T;
+    const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * T * L.ncoblk;
     L.grid = ntiles < d->sms ? ntiles : d->sms;
     const cudaError_t e = tc_launch(p.CB, L, stream);
     return e == cudaSuccess ? CC3D_OK : cuda_fail("tensor-core kernel launch", e);

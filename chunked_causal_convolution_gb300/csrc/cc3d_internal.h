@@ -39,11 +39,15 @@ struct TcLaunch {
     // tensor maps (encoded on the host)
     CUtensorMap map_x;      // x_chunk   [T][H][W][Cin]   box (CB, Sp, nrows, 1)
     CUtensorMap map_cache;  // cache_in  [P][H][W][Cin]   same box (unused if no cache)
-    CUtensorMap map_w;      // w viewed as (Cin, Cout, taps) box (CB, NT, 3)
+    CUtensorMap map_w;      // w viewed as (Cin, Cout, taps) box (CB, NT, 3 * rb)
     int T, H, W, Cin, Cout;
     int NT, nsplit, acc_stages;
+    int ncoblk;                       // output-channel blocks handled by separate tiles
     int na, nb;                       // A / B ring stages
     int prefetch;                     // temporal taps of the next tile warmed in L2 (0..3)
+    int issuers;                      // MMA-issuing warps (1 or 2)
+    int rb;                           // kernel rows (of 3 taps) per B stage: 1 or 3
+    int split_n;                      // with 2 issuers: split by N slice (else by 128-row group)
     int a_stage_bytes, b_stage_bytes;
     int tmem_cols;                    // allocated columns (power of two)
     TcGeometry g;
@@ -64,7 +68,7 @@ struct TcLaunch {
 
 // Pick tiles / pipeline depths for a tensor-core launch.  Returns false if the
 // shape has no configuration.
-bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L);
+bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, bool has_residual, TcLaunch* L);
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 
 // fp32 direct kernel (CUDA cores, fixed accumulation order).

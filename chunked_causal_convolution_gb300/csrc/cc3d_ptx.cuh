@@ -68,8 +68,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 
 // Wait until the phase with the given parity has completed.  Returns false when the
 // budget runs out or when *abort becomes non-zero (another warp already gave up).
+// After a short burst of polls the waiter sleeps `sleep_ns` between polls, so that a warp
+// waiting for a long phase (a whole tile) does not take issue slots from a busy warp on the
+// same scheduler.
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns,
-                                             const volatile int* abort)
+                                             const volatile int* abort, uint32_t sleep_ns = 0)
 {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
@@ -80,15 +83,16 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, uin
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
         if (globaltimer_ns() - t0 > budget_ns) return false;
+        if (sleep_ns) __nanosleep(sleep_ns);
     }
 }
 
 // Bounded wait done by lane 0 with the verdict broadcast to the warp (keeps control flow warp-uniform).
 __device__ __forceinline__ bool warp_bounded_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns,
-                                                  const volatile int* abort)
+                                                  const volatile int* abort, uint32_t sleep_ns = 0)
 {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = bounded_wait(bar, parity, budget_ns, abort) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = bounded_wait(bar, parity, budget_ns, abort, sleep_ns) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -106,6 +110,11 @@ __device__ __forceinline__ bool elect_one()
         : "+r"(pred)
         : "r"(0xffffffffu));
     return pred != 0;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // ---------------------------------------------------------------- TMA

@@ -15,8 +15,8 @@
 //     spatial zero padding.  Frames before the chunk come from the caller's
 //     cache (or read as zeros through a negative frame coordinate when there is
 //     no cache), which is the causal history.
-//   * B: one stage = the weights of the three taps of one (dt, dh) row for one
-//     channel block and one N slice, K-major.
+//   * B: one stage = the weights of the taps of one or all three (dt, dh) kernel
+//     rows for one channel block and one N slice, K-major.
 //
 // Warp roles (256 threads): warp 0 = TMA loader, warp 1 = MMA issuer, warp 2
 // = tensor-memory allocator and, with warp 3, the copy of the new temporal
@@ -47,18 +47,27 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxStages = 8;
 constexpr int kMaxAcc = 2;
+// sleep between polls of waits that usually last long (the epilogue waits for a whole tile), so
+// that those warps leave issue slots to the MMA warps sharing their schedulers; the loader polls
+// without sleeping (a late refill costs more than the issue slots)
+constexpr uint32_t kLoaderSleepNs = 0;
+constexpr uint32_t kEpilogueSleepNs = 256;
 
 struct TileCoord {
-    int t, w0, f0, hstart;
+    int t, w0, f0, hstart, co0;
 };
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 __device__ __forceinline__ TileCoord tile_coord(const TcLaunch& L, int tile)
 {
+    // order: frame fastest, then output-channel block (both reuse the same input windows), then
+    // the position inside the column block, then the column block
     TileCoord c;
     c.t = tile % L.T;
-    const int r = tile / L.T;
+    const int r0 = tile / L.T;
+    c.co0 = (r0 % L.ncoblk) * L.nsplit * L.NT;
+    const int r = r0 / L.ncoblk;
     const int i = r % L.g.tiles_per_cb;
     const int cbk = r / L.g.tiles_per_cb;
     c.w0 = cbk * L.g.S;
@@ -128,7 +137,32 @@ __device__ __forceinline__ void store16(const uint32_t* r, const float* s_bias, 
     }
 }
 
-template <int CB, int SUB>
+// 16 accumulator columns + bias + residual held in registers (8 bf16 pairs) -> bf16 -> global
+__device__ __forceinline__ void store16_res(const uint32_t* r, const float* s_bias, int co0, __nv_bfloat16* yp,
+                                            const uint4 ra, const uint4 rb)
+{
+    const uint32_t rr[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float lo = __fadd_rn(__fadd_rn(__uint_as_float(r[2 * k]), s_bias[co0 + 2 * k]), bf16_lo(rr[k]));
+        const float hi =
+            __fadd_rn(__fadd_rn(__uint_as_float(r[2 * k + 1]), s_bias[co0 + 2 * k + 1]), bf16_hi(rr[k]));
+        o[k] = pack_bf16x2(lo, hi);
+    }
+    reinterpret_cast<uint4*>(yp)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(yp)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// the epilogue warp is done reading this accumulator stage: let the MMA warps overwrite it
+__device__ __forceinline__ void release_acc(uint64_t* bar, int lane)
+{
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
+template <int CB, int SUBI, int RB>
 __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_constant__ TcLaunch L)
 {
     constexpr uint32_t ROWB = CB * 2;     // bytes of one pixel row of a channel block = swizzle span
@@ -144,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
     float* s_bias = reinterpret_cast<float*>(smB + (size_t)L.nb * L.b_stage_bytes);
 
     __shared__ uint64_t a_full[kMaxStages], a_empty[kMaxStages], b_full[kMaxStages], b_empty[kMaxStages];
-    __shared__ uint64_t acc_full[kMaxAcc], acc_empty[kMaxAcc], mma_drain;
+    __shared__ uint64_t acc_full[kMaxAcc], acc_empty[kMaxAcc], mma_drain[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
 
@@ -153,17 +187,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
     const int NT = L.NT;
     const int nsplit = L.nsplit;
     const int ncb = L.Cin / CB;
-    const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * L.T;
-    const int cout_pad = nsplit * NT;
+    const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * L.T * L.ncoblk;
+    const int cout_pad = L.ncoblk * nsplit * NT;
+    const int SUB = L.g.sub;                   // 128-row groups per tile (all MMA warps together)
+    const int nissue = L.issuers;              // MMA-issuing warps (1 or 2)
     const uint32_t acc_cols = (uint32_t)(SUB * nsplit * NT);
     const unsigned long long budget = L.wait_ns;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        for (int s = 0; s < L.na; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], 1); }
-        for (int s = 0; s < L.nb; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 1); }
-        for (int a = 0; a < L.acc_stages; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 4); }
-        mbar_init(&mma_drain, 1);
+        // stage releases and accumulator completions come from every MMA warp
+        for (int s = 0; s < L.na; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], nissue); }
+        for (int s = 0; s < L.nb; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], nissue); }
+        for (int a = 0; a < L.acc_stages; ++a) { mbar_init(&acc_full[a], nissue); mbar_init(&acc_empty[a], 4); }
+        mbar_init(&mma_drain[0], 1);
+        mbar_init(&mma_drain[1], 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -192,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             int last_pa[kMaxStages], last_pb[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) last_pa[s] = last_pb[s] = -1;
             const uint32_t a_tx = (uint32_t)(ROWB * Sp * L.g.nrows);
-            const uint32_t b_tx = (uint32_t)(ROWB * NT * 3);
+            const uint32_t b_tx = (uint32_t)(ROWB * NT * 3 * RB);
             bool skip_first = (L.fault == 1);
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
@@ -215,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                     int tc = tin;
                     if (tin < 0 && L.has_cache) { map = &L.map_cache; tc = tin + 2; }
                     for (int cb = 0; ok && cb < ncb; ++cb) {
-                        if (!bounded_wait(&a_empty[sa], pa ^ 1, budget, &abort_flag)) {
+                        if (!bounded_wait(&a_empty[sa], pa ^ 1, budget, &abort_flag, kLoaderSleepNs)) {
                             if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
                             ok = false;
                             break;
@@ -227,16 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                         skip_first = false;
                         last_pa[sa] = pa;
                         if (++sa == L.na) { sa = 0; pa ^= 1; }
-                        for (int dh = 0; ok && dh < 3; ++dh) {
+                        for (int dg = 0; ok && dg < 3 / RB; ++dg) {
                             for (int ns = 0; ns < nsplit; ++ns) {
-                                if (!bounded_wait(&b_empty[sb], pb ^ 1, budget, &abort_flag)) {
+                                if (!bounded_wait(&b_empty[sb], pb ^ 1, budget, &abort_flag, kLoaderSleepNs)) {
                                     if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
                                     ok = false;
                                     break;
                                 }
                                 mbar_arrive_expect_tx(&b_full[sb], b_tx);
                                 tma_load_3d(smB + (size_t)sb * L.b_stage_bytes, &L.map_w, &b_full[sb], cb * CB,
-                                            ns * NT, dt * 9 + dh * 3);
+                                            c.co0 + ns * NT, dt * 9 + dg * 3 * RB);
                                 last_pb[sb] = pb;
                                 if (++sb == L.nb) { sb = 0; pb ^= 1; }
                             }
@@ -252,10 +290,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                 if (last_pb[s] >= 0 && !bounded_wait(&b_full[s], (uint32_t)last_pb[s], budget, nullptr))
                     atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || (warp == 2 && nissue == 2)) {
+        // ------------------------------------------------------------ MMA issuers
         // The whole warp walks the loop so that every descriptor stays warp-uniform (the MMA takes
         // its operands from uniform registers); one elected lane issues each tcgen05 instruction.
+        // With two MMA warps each one owns its own accumulators (half of the 128-row groups, or one
+        // of two N slices) and both consume every stage: while one polls a barrier or does its
+        // bookkeeping the other keeps the tensor core fed.  Every accumulator is still written by
+        // one warp in program order, so the accumulation order is unchanged.
+        const int k = warp - 1;                                   // issuer index
+        const int m0 = L.split_n ? 0 : k * SUBI;                  // first 128-row group of this warp
+        const int ns_lo = L.split_n ? k : 0, ns_hi = L.split_n ? k + 1 : nsplit;
         const uint32_t idesc = make_idesc_bf16_f32(128, NT);
         const uint64_t a_desc0 = make_sdesc(smem_u32(smA), 16, SBO, LAYOUT, 0);
         const uint64_t b_desc0 = make_sdesc(smem_u32(smB), 16, SBO, LAYOUT, 0);
@@ -278,10 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             tc_fence_after();
             const uint32_t dbase = tmem + (uint32_t)as * acc_cols;
             // window row of the (dh = 0, dw = 0) view of each 128-row group, in descriptor units
-            uint32_t rowu[SUB];
+            uint32_t rowu[SUBI];
 #pragma unroll
-            for (int m = 0; m < SUB; ++m)
-                rowu[m] = (uint32_t)(c.f0 + m * L.g.sub_stride - c.hstart * Sp - Sp - 1) * ROWU;
+            for (int m = 0; m < SUBI; ++m)
+                rowu[m] = (uint32_t)(c.f0 + (m0 + m) * L.g.sub_stride - c.hstart * Sp - Sp - 1) * ROWU;
             for (int dt = 0; ok && dt < 3; ++dt) {
                 for (int cb = 0; ok && cb < ncb; ++cb) {
                     if (!warp_bounded_wait(&a_full[sa], pa, budget, &abort_flag)) {
@@ -291,9 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                     }
                     tc_fence_after();
                     const uint64_t a_st = a_desc0 + (uint64_t)(sa * a_inc);
-                    for (int dh = 0; ok && dh < 3; ++dh) {
-                        const uint64_t a_row = a_st + (uint64_t)(dh * row_shift);
-                        const bool first_row = (dt | cb | dh) == 0;
+                    for (int dg = 0; ok && dg < 3 / RB; ++dg) {
                         for (int ns = 0; ns < nsplit; ++ns) {
                             if (!warp_bounded_wait(&b_full[sb], pb, budget, &abort_flag)) {
                                 if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
@@ -302,17 +345,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                             }
                             tc_fence_after();
                             const uint64_t b_st = b_desc0 + (uint64_t)(sb * b_inc);
-                            const uint32_t dcol = dbase + (uint32_t)(ns * NT);
+                            const uint32_t dcol = dbase + (uint32_t)(ns * NT) + (uint32_t)m0 * m_cols;
+                            const bool mine = ns >= ns_lo && ns < ns_hi;
 #pragma unroll
-                            for (int dw = 0; dw < 3; ++dw) {
+                            for (int dr = 0; dr < RB; ++dr) {
+                                const int dh = dg * RB + dr;
+                                const uint64_t a_row = a_st + (uint64_t)(dh * row_shift);
+                                const bool first_row = (dt | cb | dh) == 0;
 #pragma unroll
-                                for (int m = 0; m < SUB; ++m) {
+                                for (int dw = 0; dw < 3; ++dw) {
 #pragma unroll
-                                    for (int ks = 0; ks < KSTEPS; ++ks) {
-                                        const uint64_t ad = a_row + (uint64_t)(rowu[m] + dw * ROWU + ks * 2);
-                                        const uint64_t bd = b_st + (uint64_t)(dw * b_tap_inc + ks * 2);
-                                        const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
-                                        if (elect_one()) umma_bf16_ss(dcol + (uint32_t)m * m_cols, ad, bd, idesc, acc);
+                                    for (int m = 0; m < SUBI; ++m) {
+#pragma unroll
+                                        for (int ks = 0; ks < KSTEPS; ++ks) {
+                                            const uint64_t ad = a_row + (uint64_t)(rowu[m] + dw * ROWU + ks * 2);
+                                            const uint64_t bd =
+                                                b_st + (uint64_t)((dr * 3 + dw) * b_tap_inc + ks * 2);
+                                            const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
+                                            if (mine && elect_one())
+                                                umma_bf16_ss(dcol + (uint32_t)m * m_cols, ad, bd, idesc, acc);
+                                        }
                                     }
                                 }
                             }
@@ -329,21 +381,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             if (elect_one()) umma_commit(&acc_full[as]);
         }
         // wait until every MMA this warp issued has finished writing tensor memory
-        if (elect_one()) umma_commit(&mma_drain);
+        if (elect_one()) umma_commit(&mma_drain[k]);
         __syncwarp();
-        if (!warp_bounded_wait(&mma_drain, 0, budget, nullptr) && lane == 0) atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
+        if (!warp_bounded_wait(&mma_drain[k], 0, budget, nullptr) && lane == 0)
+            atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
     } else if (warp == 2 || warp == 3) {
         // ------------------------------------------------------------ temporal cache update
-        // cache_out[j] = frame (T + j) of concat(cache_in, x); j < 2.
+        // cache_out[j] = frame (T + j) of concat(cache_in, x); j < 2.  Warps 2-3, or warp 3 alone
+        // when warp 2 issues MMAs.
+        const int cthreads = nissue == 2 ? 32 : 64;
+        const int ctid = threadIdx.x - (nissue == 2 ? 96 : 64);
         const size_t frame_chunks = (size_t)L.H * L.W * L.Cin * 2 / 16;
         const size_t total = 2 * frame_chunks;
-        const size_t gthreads = (size_t)gridDim.x * 64;
+        const size_t gthreads = (size_t)gridDim.x * cthreads;
         const uint4* xin = reinterpret_cast<const uint4*>(L.x);
         const uint4* cin = reinterpret_cast<const uint4*>(L.cache_in);
         uint4* cout_ = reinterpret_cast<uint4*>(L.cache_out);
-        // 8 independent 16-byte loads in flight per thread before their stores
-        constexpr int U = 8;
-        for (size_t i0 = ((size_t)blockIdx.x * 64 + (threadIdx.x - 64)) * U; i0 < total; i0 += gthreads * U) {
+        // 16 independent 16-byte loads in flight per thread before their stores
+        constexpr int U = 16;
+        for (size_t i0 = ((size_t)blockIdx.x * cthreads + ctid) * U; i0 < total; i0 += gthreads * U) {
             uint4 v[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -373,17 +429,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
             const int as = it % L.acc_stages;
             const int aph = (it / L.acc_stages) & 1;
+            const TileCoord c = tile_coord(L, tile);
+            // while the accumulators fill, pull this thread's residual lines into L2
+            if (res != nullptr && wide) {
+                for (int m = 0; m < SUB; ++m) {
+                    const int f = c.f0 + m * L.g.sub_stride + q * 32 + lane;
+                    const int h = f / Sp;
+                    const int jcol = f - h * Sp;
+                    const int w = c.w0 + jcol - 1;
+                    if (h < L.H && jcol >= 1 && jcol <= L.g.S && w < L.W) {
+                        const char* p = reinterpret_cast<const char*>(
+                            res + (((size_t)c.t * L.H + h) * L.W + w) * L.Cout);
+                        for (int o = 0; o < L.Cout * 2; o += 128) prefetch_l2(p + o);
+                    }
+                }
+            }
             // one lane waits and the verdict is shared: tcgen05.ld below needs the whole warp
             int ready = 0;
             if (lane == 0) {
-                ready = bounded_wait(&acc_full[as], aph, budget, &abort_flag);
+                ready = bounded_wait(&acc_full[as], aph, budget, &abort_flag, kEpilogueSleepNs);
                 if (!ready && !abort_flag) record_failure(L, STATUS_TIMEOUT_EPILOGUE, &abort_flag);
             }
             ready = __shfl_sync(0xffffffffu, ready, 0);
             if (!ready) break;
             tc_fence_after();
-            const TileCoord c = tile_coord(L, tile);
-#pragma unroll
             for (int m = 0; m < SUB; ++m) {
                 const int f = c.f0 + m * L.g.sub_stride + q * 32 + lane;
                 const int h = f / Sp;
@@ -394,27 +463,62 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                 for (int ns = 0; ns < nsplit; ++ns) {
                     const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
                                            (uint32_t)((m * nsplit + ns) * NT);
+                    const bool last_slice = (m == SUB - 1) && (ns == nsplit - 1);
+                    if (res != nullptr && wide && NT <= 128) {
+                        // narrow slices with a residual: fetch the whole residual of this output
+                        // position first, so the thread waits for memory once per slice, not per
+                        // 16 channels
+                        const int co_base = c.co0 + ns * NT;
+                        uint4 rv[16];
+                        const uint4* rp = reinterpret_cast<const uint4*>(res + px * L.Cout + co_base);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            rv[k] = (valid && k * 8 < NT) ? __ldg(rp + k) : make_uint4(0, 0, 0, 0);
+                        __nv_bfloat16* yp = y + px * L.Cout + co_base;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            if (g * 32 + 32 <= NT) {
+                                uint32_t r[32];
+                                tmem_ld_32x32b_x32(tbase + (uint32_t)(g * 32), r);
+                                tmem_ld_wait();
+                                if (last_slice && g * 32 + 32 == NT) release_acc(&acc_empty[as], lane);
+                                if (valid) {
+                                    store16_res(r, s_bias, co_base + g * 32, yp + g * 32, rv[4 * g], rv[4 * g + 1]);
+                                    store16_res(r + 16, s_bias, co_base + g * 32 + 16, yp + g * 32 + 16,
+                                                rv[4 * g + 2], rv[4 * g + 3]);
+                                }
+                            } else if (g * 32 + 16 == NT) {
+                                uint32_t r[16];
+                                tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 32), r);
+                                tmem_ld_wait();
+                                if (last_slice) release_acc(&acc_empty[as], lane);
+                                if (valid)
+                                    store16_res(r, s_bias, co_base + g * 32, yp + g * 32, rv[4 * g], rv[4 * g + 1]);
+                            }
+                        }
+                        continue;
+                    }
                     int cc = 0;
                     for (; cc + 32 <= NT; cc += 32) {
                         uint32_t r[32];
                         tmem_ld_32x32b_x32(tbase + (uint32_t)cc, r);
                         tmem_ld_wait();
+                        // the accumulators are free as soon as their last columns are in registers
+                        if (last_slice && cc + 32 == NT) release_acc(&acc_empty[as], lane);
                         if (valid) {
-                            store16(r, s_bias, ns * NT + cc, px, L.Cout, wide, res, y);
-                            store16(r + 16, s_bias, ns * NT + cc + 16, px, L.Cout, wide, res, y);
+                            store16(r, s_bias, c.co0 + ns * NT + cc, px, L.Cout, wide, res, y);
+                            store16(r + 16, s_bias, c.co0 + ns * NT + cc + 16, px, L.Cout, wide, res, y);
                         }
                     }
                     if (cc < NT) {  // NT % 32 == 16
                         uint32_t r[16];
                         tmem_ld_32x32b_x16(tbase + (uint32_t)cc, r);
                         tmem_ld_wait();
-                        if (valid) store16(r, s_bias, ns * NT + cc, px, L.Cout, wide, res, y);
+                        if (last_slice) release_acc(&acc_empty[as], lane);
+                        if (valid) store16(r, s_bias, c.co0 + ns * NT + cc, px, L.Cout, wide, res, y);
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[as]);
         }
     }
 
@@ -432,21 +536,23 @@ int env_int(const char* name, int dflt)
     return (s != nullptr && *s) ? atoi(s) : dflt;
 }
 
-template <int CB>
-void* kernel_for_sub(int sub)
+template <int CB, int RB>
+void* kernel_for(int sub)
 {
+    // sub = 128-row groups owned by one MMA warp
     switch (sub) {
-    case 1: return reinterpret_cast<void*>(tc_bf16_kernel<CB, 1>);
-    case 2: return reinterpret_cast<void*>(tc_bf16_kernel<CB, 2>);
-    case 4: return reinterpret_cast<void*>(tc_bf16_kernel<CB, 4>);
+    case 1: return reinterpret_cast<void*>(tc_bf16_kernel<CB, 1, RB>);
+    case 2: return reinterpret_cast<void*>(tc_bf16_kernel<CB, 2, RB>);
+    case 4: return reinterpret_cast<void*>(tc_bf16_kernel<CB, 4, RB>);
     default: return nullptr;
     }
 }
 
 }  // namespace
 
-bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
+bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, bool has_residual, TcLaunch* L)
 {
+    (void)has_residual;  // the measured best configuration does not depend on it today
     if (CB != 16 && CB != 32) return false;
     if (Cin % CB != 0) return false;
     L->T = T;
@@ -455,6 +561,11 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
     L->Cin = Cin;
     L->Cout = Cout;
     // output channels per MMA (N) and number of N slices
+    // Output channels: NT per MMA, nsplit N slices per tile (they share the input windows), and
+    // ncoblk channel blocks handled by different tiles.  Wide layers (more than 256 channels) are
+    // cut into channel blocks by default: the tiles then hold two 128-row groups each and load
+    // only their block's weights.
+    L->ncoblk = 1;
     if (Cout < 16) {
         L->NT = 16;
         L->nsplit = 1;
@@ -465,20 +576,48 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
         if (ns > 4) return false;
         L->nsplit = ns;
         L->NT = Cout / ns;
+        if (ns > 1 && env_int("CC3D_TC_COBLK", 1)) {
+            L->ncoblk = ns;
+            L->nsplit = 1;
+        }
     }
     const int ntot = L->NT * L->nsplit;
-    // tensor-memory budget: sub * ntot * acc_stages <= 512 columns, sub in {1, 2, 4}
-    int sub = 256 / ntot, acc = 2;
-    if (sub < 1) {
+    // 128-row groups per tile (sub) and accumulator stages (acc), within the 512 tensor-memory
+    // columns (sub * ntot * acc <= 512).  Measured on GB300: more rows per tile share each weight
+    // stage and amortise the per-stage work of the MMA warps, which outweighs double-buffering
+    // the accumulators (the epilogue is short: it reads each residual row once and frees the
+    // accumulators as soon as their last columns are in registers).
+    int sub, acc;
+    if (ntot <= 64) {
+        sub = 4;
+        acc = 2;
+    } else if (ntot <= 128) {
+        sub = 4;
         acc = 1;
-        sub = 512 / ntot;
-        if (sub < 1) return false;
+    } else if (ntot <= 256) {
+        sub = 2;
+        acc = 1;
+    } else if (ntot <= 512) {
+        sub = 1;
+        acc = 1;
+    } else {
+        return false;
     }
-    sub = sub >= 4 ? 4 : (sub >= 2 ? 2 : 1);
     sub = env_int("CC3D_TC_SUB", sub);
     acc = env_int("CC3D_TC_ACC", acc);
     if ((sub != 1 && sub != 2 && sub != 4) || acc < 1 || acc > kMaxAcc || sub * ntot * acc > 512) return false;
     L->acc_stages = acc;
+    // two MMA warps when the accumulators split evenly: by 128-row groups, else by N slices
+    L->issuers = 1;
+    L->split_n = 0;
+    if (env_int("CC3D_TC_ISSUERS", 2) == 2) {
+        if (sub >= 2) {
+            L->issuers = 2;
+        } else if (L->nsplit == 2) {
+            L->issuers = 2;
+            L->split_n = 1;
+        }
+    }
     int cols = 32;
     while (cols < sub * ntot * acc) cols *= 2;
     L->tmem_cols = cols;
@@ -512,8 +651,14 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
     const int rowb = CB * 2;
     const int a_bytes = rowb * g.Sp * g.nrows;
     L->a_stage_bytes = (a_bytes + 1023) & ~1023;
-    L->b_stage_bytes = (3 * L->NT * rowb + 1023) & ~1023;
-    const int budget = 220 * 1024 - 4 * ntot;
+    // a B stage holds the taps of `rb` kernel rows (3 or 9 taps) for one N slice: the larger
+    // stage amortises the per-stage work of the MMA warps for narrow N with four row groups
+    // (measured faster there; with two row groups the deeper 3-tap ring wins)
+    L->rb = (9 * L->NT * rowb <= 64 * 1024 && sub >= 4) ? 3 : 1;
+    L->rb = env_int("CC3D_TC_RB", L->rb);
+    if (L->rb != 1 && L->rb != 3) return false;
+    L->b_stage_bytes = (3 * L->rb * L->NT * rowb + 1023) & ~1023;
+    const int budget = 220 * 1024 - 4 * ntot * L->ncoblk;
     L->na = (L->a_stage_bytes > 40 * 1024) ? 2 : 3;
     L->na = env_int("CC3D_TC_NA", L->na);
     if (L->na < 2 || L->na > kMaxStages) return false;
@@ -532,7 +677,8 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
     // off by default: measured slower on every decoder shape (it competes with the live working set)
     L->prefetch = env_int("CC3D_TC_PREFETCH", 0);
     if (L->prefetch < 0 || L->prefetch > 3) L->prefetch = 0;
-    L->smem_bytes = (size_t)L->na * L->a_stage_bytes + (size_t)L->nb * L->b_stage_bytes + 4 * ntot + 1024;
+    L->smem_bytes =
+        (size_t)L->na * L->a_stage_bytes + (size_t)L->nb * L->b_stage_bytes + 4 * ntot * L->ncoblk + 1024;
     // one block per SM: a second resident block would wait inside its tensor-memory allocation
     if (L->smem_bytes < 120 * 1024) L->smem_bytes = 120 * 1024;
     return true;
@@ -540,7 +686,9 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, TcLaunch* L)
 
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream)
 {
-    void* kern = CB == 16 ? kernel_for_sub<16>(L.g.sub) : kernel_for_sub<32>(L.g.sub);
+    const int subi = (L.issuers == 2 && !L.split_n) ? L.g.sub / 2 : L.g.sub;
+    void* kern = CB == 16 ? (L.rb == 3 ? kernel_for<16, 3>(subi) : kernel_for<16, 1>(subi))
+                          : (L.rb == 3 ? kernel_for<32, 3>(subi) : kernel_for<32, 1>(subi));
     if (kern == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem_bytes);
     if (e != cudaSuccess) return e;

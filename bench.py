@@ -380,6 +380,39 @@ def run_ours(args, wl):
     return 0
 
 
+def run_single_chunk(args, wl):
+    """Profiling case: `n` launches of one 4-frame chunk of the workload (no JSON line)."""
+    import torch
+
+    import __graft_entry__
+    import chunked_causal_convolution_gb300 as cc3d
+    import synth
+    from synth import native
+
+    __graft_entry__.build()
+    dt = torch.bfloat16
+    T = min(4, wl.T)
+    x = native.fill_device(torch.empty((T, wl.H, wl.W, wl.Cin), dtype=dt, device="cuda"), wl.seed, synth.TID_X,
+                           wl.x)
+    w = native.fill_device(torch.empty((wl.Cout, 3, 3, 3, wl.Cin), dtype=dt, device="cuda"), wl.seed,
+                           synth.TID_W, wl.w)
+    b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device="cuda"), wl.seed, synth.TID_B, wl.b)
+    r = None
+    if wl.r is not None:
+        r = native.fill_device(torch.empty((T, wl.H, wl.W, wl.Cout), dtype=dt, device="cuda"), wl.seed,
+                               synth.TID_R, wl.r)
+    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, wl.H, wl.W)
+    cin, cout = plan.new_cache(), plan.new_cache()
+    y = torch.empty((T, wl.H, wl.W, wl.Cout), dtype=dt, device="cuda")
+    for _ in range(args.single_chunk):
+        plan.forward_chunk(x, w, b, r, cin, cout, y)
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError("device status %s" % cc3d.cc3d_status_string(st))
+    log("ran %d launches of one %d-frame chunk of %s" % (args.single_chunk, T, wl.name))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -389,6 +422,8 @@ def main():
     ap.add_argument("--workload", default="c96_residual")
     ap.add_argument("--ref-rows", type=int, default=90, help="rows of the oracle sample frame")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single-chunk", type=int, default=0,
+                    help="profiling case: run this many launches of one 4-frame chunk and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warm-up raised to 3 steps")
@@ -398,6 +433,8 @@ def main():
     if wl.T * wl.H * wl.W * max(wl.Cin, wl.Cout) * 2 > 32e9:
         log("%s does not fit resident on one device; it is covered by the streaming parity test" % wl.name)
         return 2
+    if args.single_chunk:
+        return run_single_chunk(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

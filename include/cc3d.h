@@ -16,8 +16,8 @@
  * Sources: "SwiftVR Inference Optimization" (LightX2V blog), section "ReAE:
  * Causal Halo Exchange" -- a causal layer convolves the current frame's input
  * features together with the preceding frames' input features; across chunks
- * only the previous chunk's last input frames are carried; the first chunk of
- * a video uses zeros as its history.  Section "From Pixels to Latents and
+ * only the previous chunk's last input frames are carried; a video's opening
+ * chunk starts from an all-zero history.  Section "From Pixels to Latents and
  * Back" -- long videos are processed in temporal chunks while the per-layer
  * boundary features are kept.  "SGLang-Diffusion advanced optimizations",
  * section 3 "Parallel VAE" -- the VAE's cost is dense 3-D convolution, and

@@ -12,8 +12,8 @@
  *   Exchange": a causal layer concatenates the current frame's input features
  *   with those of the preceding frame(s) and convolves the stack; across a
  *   chunk boundary the only state needed is the *input* features of the
- *   previous chunk's last frame(s); the first chunk of a video takes zeros as
- *   its history.  Section "From Pixels to Latents and Back": long videos are
+ *   previous chunk's last frame(s); a video's opening chunk starts from an
+ *   all-zero history.  Section "From Pixels to Latents and Back": long videos are
  *   split into temporal chunks and the autoencoder keeps per-layer boundary
  *   features across chunks.
  *

@@ -353,7 +353,7 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
         // weights [Cout][27][Cin] seen as (ci, co, tap) so one box holds 3 * rb K-major tap tiles
         const cuuint64_t dims[3] = {(cuuint64_t)p.Cin, (cuuint64_t)p.Cout, 27};
         const cuuint64_t strides[2] = {(cuuint64_t)27 * p.Cin * 2, (cuuint64_t)p.Cin * 2};
-        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)L.NT, (cuuint32_t)(3 * L.rb)};
+        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)(L.pair ? L.NT / 2 : L.NT), (cuuint32_t)(3 * L.rb)};
         if (g_encode(&L.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -370,7 +370,12 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     L.wait_ns = p.wait_ns;
     L.fault = p.fault;
     const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * T * L.ncoblk;
-    L.grid = ntiles < d->sms ? ntiles : d->sms;
+    if (L.pair) {
+        const int npairs = (ntiles + 1) / 2;
+        L.grid = 2 * (npairs < d->sms / 2 ? npairs : d->sms / 2);
+    } else {
+        L.grid = ntiles < d->sms ? ntiles : d->sms;
+    }
     const cudaError_t e = tc_launch(p.CB, L, stream);
     return e == cudaSuccess ? CC3D_OK : cuda_fail("tensor-core kernel launch", e);
 }

@@ -47,6 +47,7 @@ struct TcLaunch {
     int prefetch;                     // temporal taps of the next tile warmed in L2 (0..3)
     int issuers;                      // MMA-issuing warps (1 or 2)
     int rb;                           // kernel rows (of 3 taps) per B stage: 1 or 3
+    int pair;                         // 1: SM-pair kernel (cta_group::2), weight rows split in two
     int split_n;                      // with 2 issuers: split by N slice (else by 128-row group)
     int a_stage_bytes, b_stage_bytes;
     int tmem_cols;                    // allocated columns (power of two)
@@ -70,6 +71,7 @@ struct TcLaunch {
 // shape has no configuration.
 bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, bool has_residual, TcLaunch* L);
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream);
+cudaError_t tc2_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 
 // fp32 direct kernel (CUDA cores, fixed accumulation order).
 struct SimtLaunch {

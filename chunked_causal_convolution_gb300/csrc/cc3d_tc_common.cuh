@@ -1,0 +1,190 @@
+// cc3d_tc_common.cuh -- pieces shared by the one-SM and the SM-pair tensor-core kernels: tile
+// coordinates, failure recording and the epilogue's bias / residual / bf16 store helpers.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "cc3d_internal.h"
+#include "cc3d_ptx.cuh"
+
+namespace cc3d {
+namespace tcc {
+using namespace ptx;
+
+constexpr int kThreads = 256;
+constexpr int kMaxStages = 8;
+constexpr int kMaxAcc = 2;
+// sleep between polls of waits that usually last long (the epilogue waits for a whole tile), so
+// that those warps leave issue slots to the MMA warps sharing their schedulers; the loader polls
+// without sleeping (a late refill costs more than the issue slots)
+constexpr uint32_t kLoaderSleepNs = 0;
+constexpr uint32_t kEpilogueSleepNs = 256;
+
+struct TileCoord {
+    int t, w0, f0, hstart, co0;
+};
+
+__device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+__device__ __forceinline__ TileCoord tile_coord(const TcLaunch& L, int tile)
+{
+    // order: frame fastest, then output-channel block (both reuse the same input windows), then
+    // the position inside the column block, then the column block
+    TileCoord c;
+    c.t = tile % L.T;
+    const int r0 = tile / L.T;
+    c.co0 = (r0 % L.ncoblk) * L.nsplit * L.NT;
+    const int r = r0 / L.ncoblk;
+    const int i = r % L.g.tiles_per_cb;
+    const int cbk = r / L.g.tiles_per_cb;
+    c.w0 = cbk * L.g.S;
+    c.f0 = i * L.g.tile_f + (L.g.row_aligned ? 1 : 0);
+    c.hstart = floor_div(c.f0 - L.g.Sp - 1, L.g.Sp);
+    return c;
+}
+
+__device__ __forceinline__ void record_failure(const TcLaunch& L, unsigned bit, volatile int* abort_flag)
+{
+    *abort_flag = 1;
+    atomicOr(L.status, bit);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat16 l = __float2bfloat16_rn(lo);
+    const __nv_bfloat16 h = __float2bfloat16_rn(hi);
+    return (uint32_t)__bfloat16_as_ushort(l) | ((uint32_t)__bfloat16_as_ushort(h) << 16);
+}
+
+// 16 accumulator columns of one output position: + bias (+ residual) -> bf16 -> global.
+__device__ __forceinline__ void store16(const uint32_t* r, const float* s_bias, int co0, size_t px, int Cout,
+                                        bool wide, const __nv_bfloat16* res, __nv_bfloat16* y)
+{
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = __fadd_rn(__uint_as_float(r[k]), s_bias[co0 + k]);
+    if (wide) {
+        const size_t off = px * Cout + co0;
+        if (res != nullptr) {
+            const uint4 r0 = __ldg(reinterpret_cast<const uint4*>(res + off));
+            const uint4 r1 = __ldg(reinterpret_cast<const uint4*>(res + off + 8));
+            const uint32_t rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                v[2 * k] = __fadd_rn(v[2 * k], bf16_lo(rr[k]));
+                v[2 * k + 1] = __fadd_rn(v[2 * k + 1], bf16_hi(rr[k]));
+            }
+        }
+        uint4 o0, o1;
+        o0.x = pack_bf16x2(v[0], v[1]);
+        o0.y = pack_bf16x2(v[2], v[3]);
+        o0.z = pack_bf16x2(v[4], v[5]);
+        o0.w = pack_bf16x2(v[6], v[7]);
+        o1.x = pack_bf16x2(v[8], v[9]);
+        o1.y = pack_bf16x2(v[10], v[11]);
+        o1.z = pack_bf16x2(v[12], v[13]);
+        o1.w = pack_bf16x2(v[14], v[15]);
+        *reinterpret_cast<uint4*>(y + off) = o0;
+        *reinterpret_cast<uint4*>(y + off + 8) = o1;
+    } else {
+        // narrow output head: fewer than 16 channels, element stores
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int co = co0 + k;
+            if (co < Cout) {
+                const size_t off = px * Cout + co;
+                float o = v[k];
+                if (res != nullptr) o = __fadd_rn(o, __bfloat162float(res[off]));
+                y[off] = __float2bfloat16_rn(o);
+            }
+        }
+    }
+}
+
+// 16 accumulator columns + bias + residual held in registers (8 bf16 pairs) -> bf16 -> global
+__device__ __forceinline__ void store16_res(const uint32_t* r, const float* s_bias, int co0, __nv_bfloat16* yp,
+                                            const uint4 ra, const uint4 rb)
+{
+    const uint32_t rr[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float lo = __fadd_rn(__fadd_rn(__uint_as_float(r[2 * k]), s_bias[co0 + 2 * k]), bf16_lo(rr[k]));
+        const float hi =
+            __fadd_rn(__fadd_rn(__uint_as_float(r[2 * k + 1]), s_bias[co0 + 2 * k + 1]), bf16_hi(rr[k]));
+        o[k] = pack_bf16x2(lo, hi);
+    }
+    reinterpret_cast<uint4*>(yp)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(yp)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// the epilogue warp is done reading this accumulator stage: let the MMA warps overwrite it
+__device__ __forceinline__ void release_acc(uint64_t* bar, int lane)
+{
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
+// One accumulator slice of the epilogue: NT fp32 columns of this thread's output position,
+// read from tensor memory 32 (or 16) at a time, + bias (+ residual), rounded to bf16 and stored.
+// `release()` runs once, right after the last columns are in registers, when `last` is set (the
+// accumulators may then be overwritten).  With a residual and NT <= 128 the whole residual row is
+// fetched in one batch first, so the thread waits for memory once per slice.
+template <typename Release>
+__device__ __forceinline__ void epilogue_slice(uint32_t tbase, int NT, int co_base, size_t px, bool valid, bool last,
+                                               const float* s_bias, int Cout, bool wide,
+                                               const __nv_bfloat16* res, __nv_bfloat16* y, Release release)
+{
+    if (res != nullptr && wide && NT <= 128) {
+        uint4 rv[16];
+        const uint4* rp = reinterpret_cast<const uint4*>(res + px * Cout + co_base);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) rv[k] = (valid && k * 8 < NT) ? __ldg(rp + k) : make_uint4(0, 0, 0, 0);
+        __nv_bfloat16* yp = y + px * Cout + co_base;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            if (g * 32 + 32 <= NT) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + (uint32_t)(g * 32), r);
+                tmem_ld_wait();
+                if (last && g * 32 + 32 == NT) release();
+                if (valid) {
+                    store16_res(r, s_bias, co_base + g * 32, yp + g * 32, rv[4 * g], rv[4 * g + 1]);
+                    store16_res(r + 16, s_bias, co_base + g * 32 + 16, yp + g * 32 + 16, rv[4 * g + 2],
+                                rv[4 * g + 3]);
+                }
+            } else if (g * 32 + 16 == NT) {
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 32), r);
+                tmem_ld_wait();
+                if (last) release();
+                if (valid) store16_res(r, s_bias, co_base + g * 32, yp + g * 32, rv[4 * g], rv[4 * g + 1]);
+            }
+        }
+        return;
+    }
+    int cc = 0;
+    for (; cc + 32 <= NT; cc += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + (uint32_t)cc, r);
+        tmem_ld_wait();
+        if (last && cc + 32 == NT) release();
+        if (valid) {
+            store16(r, s_bias, co_base + cc, px, Cout, wide, res, y);
+            store16(r + 16, s_bias, co_base + cc + 16, px, Cout, wide, res, y);
+        }
+    }
+    if (cc < NT) {  // NT % 32 == 16
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tbase + (uint32_t)cc, r);
+        tmem_ld_wait();
+        if (last) release();
+        if (valid) store16(r, s_bias, co_base + cc, px, Cout, wide, res, y);
+    }
+}
+
+}  // namespace tcc
+}  // namespace cc3d

@@ -33,7 +33,8 @@ UNIT = "TFLOP/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tc_bf16_kernel_traffic.json")
-KERNEL_SOURCE = os.path.join(ROOT, "chunked_causal_convolution_gb300", "csrc", "cc3d_tc.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "chunked_causal_convolution_gb300", "csrc", f)
+                  for f in ("cc3d_tc.cu", "cc3d_tc2.cu", "cc3d_tc_common.cuh", "cc3d_ptx.cuh")]
 
 
 def log(*a):
@@ -50,8 +51,11 @@ def peaks():
 
 
 def kernel_source_sha():
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_per_launch(workload):
@@ -367,7 +371,7 @@ def run_ours(args, wl):
                                    "spec_2250": 100 * value / world / 2250.0},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
-                     "kernel": "tc_bf16_kernel", "flop_per_launch": flop_per_launch,
+                     "kernel": plan.kernel, "flop_per_launch": flop_per_launch,
                      "avg_launch_ms": avg_launch_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": wl.flops * world * args.steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,

@@ -19,7 +19,7 @@ __device__ unsigned g_status_word;
 
 namespace {
 
-enum KernelKind { K_SIMT_F32 = 0, K_TC_BF16 = 1, K_TC_BF16_NARROW = 2 };
+enum KernelKind { K_SIMT_F32 = 0, K_TC_BF16 = 1, K_TC_BF16_NARROW = 2, K_TC_BF16_PAIR = 3 };
 
 constexpr int kMaxDevices = 64;
 
@@ -149,7 +149,7 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
         memset(&probe, 0, sizeof(probe));
         if (!tc_configure(CB, 1, H, W, Cin, Cout, false, &probe) || !tc_configure(CB, 1, H, W, Cin, Cout, true, &probe))
             return CC3D_ERR_UNSUPPORTED;
-        kind = Cout < 16 ? K_TC_BF16_NARROW : K_TC_BF16;
+        kind = Cout < 16 ? K_TC_BF16_NARROW : (probe.pair ? K_TC_BF16_PAIR : K_TC_BF16);
     }
     cc3d_plan_s* p = new (std::nothrow) cc3d_plan_s;
     if (p == nullptr) return CC3D_ERR_OOM;
@@ -179,6 +179,7 @@ const char* cc3d_plan_kernel(cc3d_plan_t plan)
     switch (plan->kind) {
     case K_SIMT_F32: return "simt_f32";
     case K_TC_BF16: return "tc_bf16";
+    case K_TC_BF16_PAIR: return "tc_bf16_pair";
     default: return "tc_bf16_narrow";
     }
 }

@@ -123,8 +123,8 @@ const char* cc3d_last_error_detail(void);
 /* Static, human-readable text of a status code. */
 const char* cc3d_status_string(cc3d_status s);
 
-/* Name of the kernel family the plan will launch ("tc_bf16", "tc_bf16_narrow",
- * "simt_f32"); a static string, NULL for a NULL plan. */
+/* Name of the kernel family the plan will launch ("tc_bf16", "tc_bf16_pair" -- SM
+ * pairs, "tc_bf16_narrow", "simt_f32"); a static string, NULL for a NULL plan. */
 const char* cc3d_plan_kernel(cc3d_plan_t plan);
 
 /* Number of kernel launches one cc3d_forward_chunk call of this plan makes

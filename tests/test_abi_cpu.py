@@ -63,7 +63,8 @@ def test_plan_create_rejects(lib, args, code):
 
 
 @pytest.mark.parametrize("args,kernel,launches", [
-    ((96, 96, 360, 640, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
+    ((96, 96, 360, 640, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_pair", 1),
+    ((192, 192, 180, 320, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
     ((384, 384, 90, 160, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
     ((96, 3, 1440, 2560, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),
     ((16, 16, 32, 32, 3, 3, 3, cc3d.CC3D_F32), "simt_f32", 2),

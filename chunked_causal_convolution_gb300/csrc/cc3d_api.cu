@@ -1,6 +1,6 @@
 // cc3d_api.cu -- the C ABI declared in include/cc3d.h: plans, argument checks, tensor-map
 // encoding and kernel dispatch.  Nothing here computes on the host; every step of the
-// convolution runs in the kernels of cc3d_tc.cu / cc3d_simt.cu.
+// convolution runs in the kernels of cc3d_tc.cu, cc3d_tc2.cu, cc3d_head.cu and cc3d_simt.cu.
 #include <cudaTypedefs.h>
 
 #include <cstdint>
@@ -19,7 +19,7 @@ __device__ unsigned g_status_word;
 
 namespace {
 
-enum KernelKind { K_SIMT_F32 = 0, K_TC_BF16 = 1, K_TC_BF16_NARROW = 2, K_TC_BF16_PAIR = 3 };
+enum KernelKind { K_SIMT_F32 = 0, K_TC_BF16 = 1, K_TC_BF16_NARROW = 2, K_TC_BF16_PAIR = 3, K_TC_BF16_HEAD = 4 };
 
 constexpr int kMaxDevices = 64;
 
@@ -109,6 +109,65 @@ struct cc3d_plan_s {
     int fault;
 };
 
+// Narrow-output launch: tensor maps with one-row boxes for the staged input rows (loads) and the
+// new history (stores), and a (32 channels, Cout, 9 taps) box for the weights of one (dt,
+// channel block).
+static cc3d_status head_forward(const cc3d_plan_s& p, const DeviceInfo& d, int T, const void* x, const void* w,
+                                const void* b, const void* res, const void* cache_in, void* cache_out, void* y,
+                                cudaStream_t stream)
+{
+    HeadLaunch L;
+    memset(&L, 0, sizeof(L));
+    if (!head_configure(T, p.H, p.W, p.Cin, p.Cout, d.sms, &L)) return CC3D_ERR_UNSUPPORTED;
+    if (p.fault == 2) return cuda_fail("injected tensor-map encode failure");  // nothing launched
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const cuuint64_t strides[3] = {(cuuint64_t)p.Cin * 2, (cuuint64_t)p.W * p.Cin * 2,
+                                   (cuuint64_t)p.H * p.W * p.Cin * 2};
+    const cuuint32_t box[4] = {32, 136, 1, 1};
+    const cuuint64_t dims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)T};
+    if (g_encode(&L.map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cuda_fail("cuTensorMapEncodeTiled (x_chunk)");
+    if (cache_in != nullptr) {
+        const cuuint64_t cdims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, 2};
+        if (g_encode(&L.map_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache_in), cdims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_fail("cuTensorMapEncodeTiled (cache_in)");
+    }
+    {
+        const cuuint64_t cdims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, 2};
+        const cuuint32_t sbox[4] = {32, 126, 1, 1};
+        if (g_encode(&L.map_cache_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache_out, cdims, strides, sbox, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_fail("cuTensorMapEncodeTiled (cache_out)");
+    }
+    {
+        // weights [Cout][27][Cin] seen as (ci, co, tap): one box = the 9 spatial taps of one dt
+        const cuuint64_t wdims[3] = {(cuuint64_t)p.Cin, (cuuint64_t)p.Cout, 27};
+        const cuuint64_t wstrides[2] = {(cuuint64_t)27 * p.Cin * 2, (cuuint64_t)p.Cin * 2};
+        const cuuint32_t wbox[3] = {32, (cuuint32_t)p.Cout, 9};
+        if (g_encode(&L.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), wdims, wstrides, wbox, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_fail("cuTensorMapEncodeTiled (w)");
+    }
+    L.has_cache = cache_in != nullptr;
+    L.bias = b;
+    L.res = res;
+    L.y = y;
+    L.x = x;
+    L.cache_in = cache_in;
+    L.cache_out = cache_out;
+    L.status = d.status;
+    L.wait_ns = p.wait_ns;
+    L.fault = p.fault;
+    const cudaError_t e = head_launch(L, stream);
+    return e == cudaSuccess ? CC3D_OK : cuda_fail("narrow-output kernel launch", e);
+}
+
 extern "C" {
 
 const char* cc3d_status_string(cc3d_status s)
@@ -145,11 +204,18 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
         if (Cin % 16 != 0 || Cin > 1024) return CC3D_ERR_UNSUPPORTED;
         if (!(Cout < 16 || (Cout % 16 == 0 && Cout <= 512))) return CC3D_ERR_UNSUPPORTED;
         CB = (Cin % 32 == 0) ? 32 : 16;
-        TcLaunch probe;
-        memset(&probe, 0, sizeof(probe));
-        if (!tc_configure(CB, 1, H, W, Cin, Cout, false, &probe) || !tc_configure(CB, 1, H, W, Cin, Cout, true, &probe))
-            return CC3D_ERR_UNSUPPORTED;
-        kind = Cout < 16 ? K_TC_BF16_NARROW : (probe.pair ? K_TC_BF16_PAIR : K_TC_BF16);
+        HeadLaunch hprobe;
+        memset(&hprobe, 0, sizeof(hprobe));
+        if (head_configure(1, H, W, Cin, Cout, 1, &hprobe)) {
+            kind = K_TC_BF16_HEAD;  // narrow output: taps stacked into N
+        } else {
+            TcLaunch probe;
+            memset(&probe, 0, sizeof(probe));
+            if (!tc_configure(CB, 1, H, W, Cin, Cout, false, &probe) ||
+                !tc_configure(CB, 1, H, W, Cin, Cout, true, &probe))
+                return CC3D_ERR_UNSUPPORTED;
+            kind = Cout < 16 ? K_TC_BF16_NARROW : (probe.pair ? K_TC_BF16_PAIR : K_TC_BF16);
+        }
     }
     cc3d_plan_s* p = new (std::nothrow) cc3d_plan_s;
     if (p == nullptr) return CC3D_ERR_OOM;
@@ -180,6 +246,7 @@ const char* cc3d_plan_kernel(cc3d_plan_t plan)
     case K_SIMT_F32: return "simt_f32";
     case K_TC_BF16: return "tc_bf16";
     case K_TC_BF16_PAIR: return "tc_bf16_pair";
+    case K_TC_BF16_HEAD: return "tc_bf16_head";
     default: return "tc_bf16_narrow";
     }
 }
@@ -323,6 +390,8 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
             return cuda_fail("cache update launch", e);
         return CC3D_OK;
     }
+
+    if (p.kind == K_TC_BF16_HEAD) return head_forward(p, *d, T, x, w, b, res, cache_in, cache_out, y, stream);
 
     // ---- tensor-core path
     TcLaunch L;

@@ -12,6 +12,7 @@ enum : unsigned {
     STATUS_TIMEOUT_MMA = 1u << 1,
     STATUS_TIMEOUT_EPILOGUE = 1u << 2,
     STATUS_TIMEOUT_DRAIN = 1u << 3,
+    STATUS_TIMEOUT_COPY = 1u << 4,
 };
 
 // Geometry of the tensor-core kernel's tiles.
@@ -72,6 +73,35 @@ struct TcLaunch {
 bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, bool has_residual, TcLaunch* L);
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 cudaError_t tc2_launch(int CB, const TcLaunch& L, cudaStream_t stream);
+
+// Narrow-output kernel (Cout <= 5): the nine spatial taps stacked into N, rows streamed once.
+struct HeadLaunch {
+    CUtensorMap map_x;          // x_chunk   [T][H][W][Cin]  box (32, 136, 1, 1)
+    CUtensorMap map_cache;      // cache_in  [2][H][W][Cin]  same box (unused if no cache)
+    CUtensorMap map_w;          // w viewed as (Cin, Cout, 27 taps)  box (32, Cout, 9)
+    CUtensorMap map_cache_out;  // cache_out [2][H][W][Cin]  box (32, 126, 1, 1), stored from shared memory
+    int T, H, W, Cin, Cout;
+    int gmax;               // output frames per pass over the rows
+    int ncolblk;            // column strips of 126 output pixels
+    long long units;        // (frame group, strip, output row) units, dealt out in equal runs
+    int nstages;            // input-row stages in shared memory
+    int w_bytes, x_stage_bytes;
+    int tmem_cols;
+    int has_cache;
+    const void* bias;       // bf16 [Cout] or null
+    const void* res;        // bf16 [T][H][W][Cout] or null
+    void* y;                // bf16 [T][H][W][Cout]
+    const void* x;
+    const void* cache_in;
+    void* cache_out;
+    unsigned* status;
+    unsigned long long wait_ns;
+    int fault;
+    int grid;
+    size_t smem_bytes;
+};
+bool head_configure(int T, int H, int W, int Cin, int Cout, int sms, HeadLaunch* L);
+cudaError_t head_launch(const HeadLaunch& L, cudaStream_t stream);
 
 // fp32 direct kernel (CUDA cores, fixed accumulation order).
 struct SimtLaunch {

@@ -66,21 +66,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread is parked by the hardware until the phase
+// completes or about hint_ns have passed, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        "  .reg .pred p;\n"
+        "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "  selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// longest time a waiting thread stays parked before it re-checks the budget and the abort flag
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Wait until the phase with the given parity has completed.  Returns false when the
 // budget runs out or when *abort becomes non-zero (another warp already gave up).
-// After a short burst of polls the waiter sleeps `sleep_ns` between polls, so that a warp
-// waiting for a long phase (a whole tile) does not take issue slots from a busy warp on the
-// same scheduler.
+// The waiter is suspended by the hardware between checks: tight polling loops of several
+// waiting warps would otherwise crowd the shared-memory pipe that every mbarrier operation,
+// shared load and tensor-core issue of the busy warps goes through.  `sleep_ns` adds a pause
+// after a check that found the phase still open.
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns,
                                              const volatile int* abort, uint32_t sleep_ns = 0)
 {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_hint(bar, parity, kSuspendHintNs)) return true;
         if (abort && *abort) return false;
         if (globaltimer_ns() - t0 > budget_ns) return false;
         if (sleep_ns) __nanosleep(sleep_ns);
@@ -94,6 +113,12 @@ __device__ __forceinline__ bool warp_bounded_wait(uint64_t* bar, uint32_t parity
     int ok = 0;
     if ((threadIdx.x & 31) == 0) ok = bounded_wait(bar, parity, budget_ns, abort, sleep_ns) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Barrier over a subset of the block's warps (ids 1..15; id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // true in exactly one lane of the (fully active) warp

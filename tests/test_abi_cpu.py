@@ -66,7 +66,10 @@ def test_plan_create_rejects(lib, args, code):
     ((96, 96, 360, 640, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_pair", 1),
     ((192, 192, 180, 320, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
     ((384, 384, 90, 160, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
-    ((96, 3, 1440, 2560, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),
+    ((96, 3, 1440, 2560, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_head", 1),
+    ((48, 3, 64, 64, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),   # Cin not a multiple of 32
+    ((512, 3, 64, 64, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),  # too wide to stage a row
+    ((96, 8, 64, 64, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),   # 9 taps x 8 channels exceed N = 48
     ((16, 16, 32, 32, 3, 3, 3, cc3d.CC3D_F32), "simt_f32", 2),
     ((3, 5, 7, 9, 2, 1, 3, cc3d.CC3D_F32), "simt_f32", 2),
 ])

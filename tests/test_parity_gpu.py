@@ -41,11 +41,27 @@ SMALL = [
     ("bf16_flat", "bf16", 64, 64, 3, 7, 100, [1, 2], True, False),
     ("bf16_split_n", "bf16", 32, 384, 3, 4, 40, [3], False, True),
     ("bf16_narrow_head", "bf16", 96, 3, 3, 6, 130, [2, 1], True, True),
+    ("bf16_head_strips_rows", "bf16", 64, 3, 5, 21, 260, [4, 1], True, False),
+    ("bf16_head_cout1_two_passes", "bf16", 32, 1, 10, 5, 40, [10], True, True),
+    ("bf16_head_cout5_cin256", "bf16", 256, 5, 7, 4, 127, [6, 1], False, True),
+    ("bf16_head_cout2", "bf16", 160, 2, 3, 3, 253, [1, 2], True, False),
+    ("bf16_narrow_generic", "bf16", 48, 3, 3, 5, 70, [2, 1], True, True),
     ("bf16_cb16", "bf16", 16, 32, 4, 9, 17, [1, 1, 2], True, False),
     ("bf16_two_flat_blocks", "bf16", 32, 16, 2, 3, 300, [2], True, False),
     ("bf16_c192_like", "bf16", 192, 192, 3, 8, 64, [2, 1], True, False),
     ("bf16_one_pixel", "bf16", 32, 32, 3, 1, 1, [1, 1, 1], True, True),
 ]
+
+
+# the kernel family each small case exercises
+SMALL_KERNEL = {
+    "tiny_f32_workload": "simt_f32", "f32_odd_shape": "simt_f32",
+    "bf16_row_aligned_residual": "tc_bf16_pair", "bf16_flat": "tc_bf16", "bf16_split_n": "tc_bf16",
+    "bf16_narrow_head": "tc_bf16_head", "bf16_head_strips_rows": "tc_bf16_head",
+    "bf16_head_cout1_two_passes": "tc_bf16_head", "bf16_head_cout5_cin256": "tc_bf16_head",
+    "bf16_head_cout2": "tc_bf16_head", "bf16_narrow_generic": "tc_bf16_narrow", "bf16_cb16": "tc_bf16",
+    "bf16_two_flat_blocks": "tc_bf16", "bf16_c192_like": "tc_bf16", "bf16_one_pixel": "tc_bf16",
+}
 
 
 def _small_case(name, dtype, Cin, Cout, T, H, W, chunks, bias, residual):
@@ -61,6 +77,7 @@ def _small_case(name, dtype, Cin, Cout, T, H, W, chunks, bias, residual):
 def test_small_shapes_match_oracle_elementwise(case):
     name, dtype, Cin, Cout, T, H, W, chunks, bias, residual = case
     raw, dev, plan = _small_case(*case)
+    assert plan.kernel == SMALL_KERNEL[name]
     y, caches = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), chunks)
     assert plan.status() == 0
     ref = oracle.conv_whole(to_f64(raw["x"], dtype), to_f64(raw["w"], dtype),

@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
     constexpr uint32_t ROWB = kHeadCB * 2;
     constexpr uint32_t SBO = 8 * ROWB;
     constexpr int KSTEPS = kHeadCB / 16;
-    constexpr int EBUF = GMAX * 4 * 2 * kHeadEdge;  // floats per edge buffer
+    constexpr int EBUF = GMAX * 6 * 2 * kHeadEdge;  // floats per edge buffer: [frame][slot 0..5][side]
 
     extern __shared__ uint8_t dsm_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
             reinterpret_cast<uint4*>(tile)[i % pad16] = make_uint4(0, 0, 0, 0);
         }
     }
+    for (int i = threadIdx.x; i < 2 * EBUF; i += kThreads) s_edge[i] = 0.0f;  // slots 0 and 5 stay zero
     if (threadIdx.x < 8) {
         const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(L.bias);
         s_bias[threadIdx.x] = (b != nullptr && (int)threadIdx.x < COUT) ? __bfloat162float(b[threadIdx.x]) : 0.0f;
@@ -318,6 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
         const int p = q * 32 + lane;
         const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(L.res);
         __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(L.y);
+        float bias[COUT];
+#pragma unroll
+        for (int c = 0; c < COUT; ++c) bias[c] = s_bias[c];
+        // edge lanes publish into slot q + 1; a lane 0 reads its left terms from slot q and a lane 31
+        // its right terms from slot q + 2 (slots 0 and 5 stay zero: there is no warp -1 or 4)
+        const bool edge_lane = lane == 0 || lane == 31;
+        const int side = lane == 0 ? 1 : 0;
         uint32_t rs = 0;
         bool ok = true;
         for (long long u = ubeg; ok && u < uend;) {
@@ -345,27 +353,20 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
                 const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + slot * SLOT;
                 if (ready) {
                     tc_fence_after();
-                    // publish the edge lanes' terms for the neighbouring warps
+                    // publish the edge lanes' terms (lane 31: dw = 0, lane 0: dw = 2) for the neighbours
 #pragma unroll
                     for (int t = 0; t < GMAX; ++t) {
                         if (t < g.G) {
                             uint32_t v[NCOL];
                             tmem_ld_cols<NCOL>(trow + (uint32_t)(t * NCOL), v);
-                            float* e = eb + ((t * 4 + q) * 2) * kHeadEdge;
-                            if (lane == 31) {
+                            float* e = eb + ((t * 6 + q + 1) * 2 + side) * kHeadEdge;
 #pragma unroll
-                                for (int dh = 0; dh < 3; ++dh)
+                            for (int dh = 0; dh < 3; ++dh)
 #pragma unroll
-                                    for (int c = 0; c < COUT; ++c)
-                                        e[dh * COUT + c] = __uint_as_float(v[(dh * 3 + 0) * COUT + c]);
-                            }
-                            if (lane == 0) {
-#pragma unroll
-                                for (int dh = 0; dh < 3; ++dh)
-#pragma unroll
-                                    for (int c = 0; c < COUT; ++c)
-                                        e[kHeadEdge + dh * COUT + c] = __uint_as_float(v[(dh * 3 + 2) * COUT + c]);
-                            }
+                                for (int c = 0; c < COUT; ++c) {
+                                    const uint32_t val = lane == 0 ? v[(dh * 3 + 2) * COUT + c] : v[(dh * 3) * COUT + c];
+                                    if (edge_lane) e[dh * COUT + c] = __uint_as_float(val);
+                                }
                         }
                     }
                 }
@@ -380,17 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
 #pragma unroll
                 for (int t = 0; t < GMAX; ++t) {
                     if (t < g.G) {
-                        size_t px = 0;
+                        const long long px = ((long long)(g.t0 + t) * L.H + h) * L.W + w;  // used only if store
                         float rr[COUT];
 #pragma unroll
-                        for (int c = 0; c < COUT; ++c) rr[c] = 0.0f;
-                        if (store) {
-                            px = ((size_t)(g.t0 + t) * L.H + h) * L.W + w;
-                            if (res != nullptr) {
-#pragma unroll
-                                for (int c = 0; c < COUT; ++c) rr[c] = __bfloat162float(res[px * COUT + c]);
-                            }
-                        }
+                        for (int c = 0; c < COUT; ++c)
+                            rr[c] = (store && res != nullptr) ? __bfloat162float(res[px * COUT + c]) : 0.0f;
                         uint32_t v[NCOL];
                         tmem_ld_cols<NCOL>(trow + (uint32_t)(t * NCOL), v);
                         if (t == g.G - 1) {
@@ -399,9 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&acc_empty[slot]);
                         }
-                        // warp q - 1's lane 31 and warp q + 1's lane 0 (clamped: read only when those exist)
-                        const float* el = eb + ((t * 4 + (q > 0 ? q - 1 : 0)) * 2) * kHeadEdge;
-                        const float* er = eb + ((t * 4 + (q < 3 ? q + 1 : 3)) * 2 + 1) * kHeadEdge;
+                        // the neighbours' edge terms: same address in every lane (a broadcast read)
+                        float el[16], er[16];  // 3 * COUT <= 15 terms per side
+                        const float4* el4 = reinterpret_cast<const float4*>(eb + ((t * 6 + q) * 2 + 0) * kHeadEdge);
+                        const float4* er4 = reinterpret_cast<const float4*>(eb + ((t * 6 + q + 2) * 2 + 1) * kHeadEdge);
+#pragma unroll
+                        for (int k4 = 0; k4 < (3 * COUT + 3) / 4; ++k4) {
+                            const float4 a = el4[k4], b = er4[k4];
+                            el[4 * k4] = a.x; el[4 * k4 + 1] = a.y; el[4 * k4 + 2] = a.z; el[4 * k4 + 3] = a.w;
+                            er[4 * k4] = b.x; er[4 * k4 + 1] = b.y; er[4 * k4 + 2] = b.z; er[4 * k4 + 3] = b.w;
+                        }
                         float sdh[3][COUT];
 #pragma unroll
                         for (int dh = 0; dh < 3; ++dh) {
@@ -409,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
                             for (int c = 0; c < COUT; ++c) {
                                 float l = __shfl_up_sync(0xffffffffu, __uint_as_float(v[(dh * 3 + 0) * COUT + c]), 1);
                                 float r = __shfl_down_sync(0xffffffffu, __uint_as_float(v[(dh * 3 + 2) * COUT + c]), 1);
-                                if (lane == 0) l = q > 0 ? el[dh * COUT + c] : 0.0f;
-                                if (lane == 31) r = q < 3 ? er[dh * COUT + c] : 0.0f;
+                                l = lane == 0 ? el[dh * COUT + c] : l;
+                                r = lane == 31 ? er[dh * COUT + c] : r;
                                 sdh[dh][c] = __fadd_rn(__fadd_rn(l, __uint_as_float(v[(dh * 3 + 1) * COUT + c])), r);
                             }
                         }
@@ -419,11 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
                             const float done = __fadd_rn(P[t][c], sdh[2][c]);
                             P[t][c] = __fadd_rn(Q[t][c], sdh[1][c]);
                             Q[t][c] = sdh[0][c];
-                            if (store) {
-                                float o = __fadd_rn(done, s_bias[c]);
-                                if (res != nullptr) o = __fadd_rn(o, rr[c]);
-                                y[px * COUT + c] = __float2bfloat16_rn(o);
-                            }
+                            const float o = __fadd_rn(__fadd_rn(done, bias[c]), rr[c]);
+                            if (store) y[px * COUT + c] = __float2bfloat16_rn(o);
                         }
                     }
                 }
@@ -458,7 +457,7 @@ bool head_configure(int T, int H, int W, int Cin, int Cout, int sms, HeadLaunch*
     const int ncb = Cin / kHeadCB;
     L->w_bytes = (3 * ncb * ncol * kHeadCB * 2 + 1023) & ~1023;
     L->x_stage_bytes = ncb * kHeadBox * kHeadCB * 2;  // a multiple of 512 B (the 64-byte swizzle atom)
-    const int edge_bytes = 2 * L->gmax * 4 * 2 * kHeadEdge * 4;
+    const int edge_bytes = 2 * L->gmax * 6 * 2 * kHeadEdge * 4;
     const int fixed = L->w_bytes + edge_bytes + 1024;  // + alignment slack
     int nst = (227 * 1024 - fixed) / L->x_stage_bytes;
     if (nst > kHeadMaxStages) nst = kHeadMaxStages;

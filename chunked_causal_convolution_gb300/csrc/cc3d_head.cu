@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
         // warp 1 owns the even output frames of a pass, warp 2 the odd ones: every accumulator
         // (input row, output frame) has one writer, in the order dt, channel block, k step.
         const int k = warp - 1;
+        const bool lead = lane == 0;  // issues every MMA and commit: the lane that polls the barriers
         const uint32_t idesc = make_idesc_bf16_f32(128, NCOL);
         // the A operand starts at staged row 7 (position w0 - 1); the swizzle follows the address bits
         const uint64_t x_desc0 = make_sdesc(smem_u32(smX) + (kHeadLead - 1) * ROWB, 16, SBO, LAYOUT_SW64, 0);
@@ -234,26 +235,26 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t xs = x_desc0 + (uint64_t)(s * x_inc);
+                    const uint64_t xs = desc_add(x_desc0, s * x_inc);
                     bool any = false;
                     for (int dt = 0; dt < 3; ++dt) {
                         const int tout = j - dt;  // input frame t0 - 2 + j is tap dt of output frame t0 + tout
                         if (tout < 0 || tout >= g.G || (tout & 1) != k) continue;
                         const uint32_t d = tmem + slot * SLOT + (uint32_t)(tout * NCOL);
-                        const uint64_t wd = w_desc0 + (uint64_t)(dt * ncb) * w_inc;
+                        const uint64_t wd = desc_add(w_desc0, dt * ncb * w_inc);
                         for (int cb = 0; cb < ncb; ++cb) {
 #pragma unroll
                             for (int ks = 0; ks < KSTEPS; ++ks) {
-                                const uint64_t ad = xs + (uint64_t)(cb * cb_inc + ks * 2);
-                                const uint64_t bd = wd + (uint64_t)(cb * w_inc + ks * 2);
+                                const uint64_t ad = desc_add(xs, cb * cb_inc + ks * 2);
+                                const uint64_t bd = desc_add(wd, cb * w_inc + ks * 2);
                                 const uint32_t acc = (dt == 0 && cb == 0 && ks == 0) ? 0u : 1u;
-                                if (elect_one()) umma_bf16_ss(d, ad, bd, idesc, acc);
+                                if (lead) umma_bf16_ss(d, ad, bd, idesc, acc);
                             }
                         }
                         any = true;
                     }
                     // a warp that read nothing from this stage releases it at once
-                    if (elect_one()) {
+                    if (lead) {
                         if (any) umma_commit(&x_empty[s]);
                         else mbar_arrive(&x_empty[s]);
                     }
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
                     if (++s == nst) { s = 0; ph ^= 1; }
                 }
                 if (!ok) break;
-                if (elect_one()) {
+                if (lead) {
                     if (wrote) umma_commit(&acc_full[slot]);
                     else mbar_arrive(&acc_full[slot]);
                 }
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
             }
             u += g.h1 - g.h0;
         }
-        if (elect_one()) umma_commit(&mma_drain[k]);
+        if (lead) umma_commit(&mma_drain[k]);
         __syncwarp();
         if (!warp_bounded_wait(&mma_drain[k], 0, budget, nullptr) && lane == 0)
             atomicOr(L.status, STATUS_TIMEOUT_DRAIN);

@@ -397,6 +397,13 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t mask)
 // swizzle layout (bits 61-63: 0 none, 2 = 128B, 4 = 64B, 6 = 32B).
 enum : uint32_t { LAYOUT_NONE = 0, LAYOUT_SW128 = 2, LAYOUT_SW64 = 4, LAYOUT_SW32 = 6 };
 
+// Descriptor plus an offset in 16-byte units: the start-address and leading-offset fields are in
+// the low word and no offset used here carries out of it, so a 32-bit add suffices.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off)
+{
+    return (d & 0xFFFFFFFF00000000ull) | (uint64_t)((uint32_t)d + off);
+}
+
 __host__ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
                                                         uint32_t layout, uint32_t base_offset)
 {

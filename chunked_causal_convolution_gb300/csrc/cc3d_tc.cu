@@ -24,11 +24,12 @@
 // [+ residual] -> bf16 -> global), one output position per thread.
 //
 // The MMA warp keeps the shared-memory descriptors of stage 0 and advances
-// them by additions only (the start-address field is the low 14 bits and every
-// address stays below 2^18 bytes), with the tap / row-group / K-step loops
-// unrolled at compile time.  All 32 lanes walk the issue loop, so the
-// descriptors stay warp-uniform, and an elected lane issues each MMA: issuing
-// from a single divergent lane instead costs about 1.6x the time per MMA.
+// them by 32-bit additions on the low word (the start-address field is the low
+// 14 bits and every address stays below 2^18 bytes), with the tap / row-group /
+// K-step loops unrolled at compile time.  All 32 lanes walk the issue loop, so
+// the descriptors stay warp-uniform, and lane 0 -- the lane that polls the
+// barriers -- issues every MMA (an elect.sync before every MMA made the warp
+// reconverge each time and cost about 10 % end to end).
 //
 // The accumulation order of every output is fixed: dt, channel block, dh, dw,
 // 16-channel step -- it depends neither on the tile an output falls in nor on
@@ -177,12 +178,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
     } else if (warp == 1 || (warp == 2 && nissue == 2)) {
         // ------------------------------------------------------------ MMA issuers
         // The whole warp walks the loop so that every descriptor stays warp-uniform (the MMA takes
-        // its operands from uniform registers); one elected lane issues each tcgen05 instruction.
+        // its operands from uniform registers); lane 0 issues the tcgen05 instructions.
         // With two MMA warps each one owns its own accumulators (half of the 128-row groups, or one
         // of two N slices) and both consume every stage: while one polls a barrier or does its
         // bookkeeping the other keeps the tensor core fed.  Every accumulator is still written by
         // one warp in program order, so the accumulation order is unchanged.
-        const int k = warp - 1;                                   // issuer index
+        const int k = warp - 1;
+        // Lane 0 issues every MMA and commit of this warp: it is the lane that polls the full
+        // barriers (warp_bounded_wait), so the thread that observes a stage's completion is the one
+        // whose MMAs read it, and a commit tracks the MMAs of the thread that issues it.  (An
+        // elect.sync per MMA made the warp reconverge before every instruction and was measured
+        // 10 % slower; a lane elected once need not be the polling lane, and that form gave wrong
+        // results on first launches.)
+        const bool lead = lane == 0;                                   // issuer index
         const int m0 = L.split_n ? 0 : k * SUBI;                  // first 128-row group of this warp
         const int ns_lo = L.split_n ? k : 0, ns_hi = L.split_n ? k + 1 : nsplit;
         const uint32_t idesc = make_idesc_bf16_f32(128, NT);
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
 #pragma unroll
                             for (int dr = 0; dr < RB; ++dr) {
                                 const int dh = dg * RB + dr;
-                                const uint64_t a_row = a_st + (uint64_t)(dh * row_shift);
+                                const uint64_t a_row = desc_add(a_st, dh * row_shift);
                                 const bool first_row = (dt | cb | dh) == 0;
 #pragma unroll
                                 for (int dw = 0; dw < 3; ++dw) {
@@ -242,30 +250,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                                     for (int m = 0; m < SUBI; ++m) {
 #pragma unroll
                                         for (int ks = 0; ks < KSTEPS; ++ks) {
-                                            const uint64_t ad = a_row + (uint64_t)(rowu[m] + dw * ROWU + ks * 2);
-                                            const uint64_t bd =
-                                                b_st + (uint64_t)((dr * 3 + dw) * b_tap_inc + ks * 2);
+                                            const uint64_t ad = desc_add(a_row, rowu[m] + dw * ROWU + ks * 2);
+                                            const uint64_t bd = desc_add(b_st, (dr * 3 + dw) * b_tap_inc + ks * 2);
                                             const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
-                                            if (mine && elect_one())
+                                            if (mine && lead)
                                                 umma_bf16_ss(dcol + (uint32_t)m * m_cols, ad, bd, idesc, acc);
                                         }
                                     }
                                 }
                             }
-                            if (elect_one()) umma_commit(&b_empty[sb]);
+                            if (lead) umma_commit(&b_empty[sb]);
+                            __syncwarp();
                             if (++sb == L.nb) { sb = 0; pb ^= 1; }
                         }
                     }
                     if (!ok) break;
-                    if (elect_one()) umma_commit(&a_empty[sa]);
+                    if (lead) umma_commit(&a_empty[sa]);
                     if (++sa == L.na) { sa = 0; pa ^= 1; }
                 }
             }
             if (!ok) break;
-            if (elect_one()) umma_commit(&acc_full[as]);
+            if (lead) umma_commit(&acc_full[as]);
         }
         // wait until every MMA this warp issued has finished writing tensor memory
-        if (elect_one()) umma_commit(&mma_drain[k]);
+        if (lead) umma_commit(&mma_drain[k]);
         __syncwarp();
         if (!warp_bounded_wait(&mma_drain[k], 0, budget, nullptr) && lane == 0)
             atomicOr(L.status, STATUS_TIMEOUT_DRAIN);

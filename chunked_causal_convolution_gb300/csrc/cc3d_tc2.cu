@@ -163,6 +163,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (leader && (warp == 1 || (warp == 2 && nissue == 2))) {
         // ------------------------------------------------------------ MMA issuers (leader only)
         const int k = warp - 1;
+        // Lane 0 issues every MMA and commit of this warp: it is the lane that polls the full
+        // barriers (warp_bounded_wait), so the thread that observes a stage's completion is the one
+        // whose MMAs read it, and a commit tracks the MMAs of the thread that issues it.  (An
+        // elect.sync per MMA made the warp reconverge before every instruction and was measured
+        // 10 % slower; a lane elected once need not be the polling lane, and that form gave wrong
+        // results on first launches.)
+        const bool lead = lane == 0;
         const int m0 = L.split_n ? 0 : k * SUBI;
         const int ns_lo = L.split_n ? k : 0, ns_hi = L.split_n ? k + 1 : nsplit;
         const uint32_t idesc = make_idesc_bf16_f32(256, NT);
@@ -214,7 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int dr = 0; dr < RB; ++dr) {
                                 const int dh = dg * RB + dr;
-                                const uint64_t a_row = a_st + (uint64_t)(dh * row_shift);
+                                const uint64_t a_row = desc_add(a_st, dh * row_shift);
                                 const bool first_row = (dt | cb | dh) == 0;
 #pragma unroll
                                 for (int dw = 0; dw < 3; ++dw) {
@@ -222,29 +229,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     for (int m = 0; m < SUBI; ++m) {
 #pragma unroll
                                         for (int ks = 0; ks < KSTEPS; ++ks) {
-                                            const uint64_t ad = a_row + (uint64_t)(rowu[m] + dw * ROWU + ks * 2);
-                                            const uint64_t bd =
-                                                b_st + (uint64_t)((dr * 3 + dw) * b_tap_inc + ks * 2);
+                                            const uint64_t ad = desc_add(a_row, rowu[m] + dw * ROWU + ks * 2);
+                                            const uint64_t bd = desc_add(b_st, (dr * 3 + dw) * b_tap_inc + ks * 2);
                                             const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
-                                            if (mine && elect_one())
+                                            if (mine && lead)
                                                 umma_bf16_ss_pair(dcol + (uint32_t)m * m_cols, ad, bd, idesc, acc);
                                         }
                                     }
                                 }
                             }
-                            if (elect_one()) umma_commit_pair(&b_empty[sb], 3);
+                            if (lead) umma_commit_pair(&b_empty[sb], 3);
+                            __syncwarp();
                             if (++sb == L.nb) { sb = 0; pb ^= 1; }
                         }
                     }
                     if (!ok) break;
-                    if (elect_one()) umma_commit_pair(&a_empty[sa], 3);
+                    if (lead) umma_commit_pair(&a_empty[sa], 3);
                     if (++sa == L.na) { sa = 0; pa ^= 1; }
                 }
             }
             if (!ok) break;
-            if (elect_one()) umma_commit_pair(&acc_full[as], 3);
+            if (lead) umma_commit_pair(&acc_full[as], 3);
         }
-        if (elect_one()) umma_commit_pair(&mma_drain[k], 1);
+        if (lead) umma_commit_pair(&mma_drain[k], 1);
         __syncwarp();
         if (!warp_bounded_wait(&mma_drain[k], 0, budget, nullptr) && lane == 0)
             atomicOr(L.status, STATUS_TIMEOUT_DRAIN);

@@ -99,6 +99,18 @@ def test_small_shapes_match_oracle_elementwise(case):
     for alt in ([T], [1] * T):
         y2, _ = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), alt)
         assert torch.equal(y2, y), (name, alt)
+    # a second input set right after the first: a stage consumed before its copy landed would
+    # still hold the first set's data (repeated launches on equal inputs cannot show that)
+    x_dist = synth.Dist.uniform(-1.0, 1.0) if name == "tiny_f32_workload" else None
+    raw2 = small_inputs(Cin, Cout, T, H, W, dtype, 5000 + len(name), bias, residual, x_dist=x_dist)
+    dev2 = {k: to_device(v, dtype) for k, v in raw2.items()}
+    y3, _ = run_chunks(plan, dev2["x"], dev2["w"], dev2.get("b"), dev2.get("r"), chunks)
+    assert plan.status() == 0
+    ref2 = oracle.conv_whole(to_f64(raw2["x"], dtype), to_f64(raw2["w"], dtype),
+                             to_f64(raw2["b"], dtype) if bias else None,
+                             to_f64(raw2["r"], dtype) if residual else None)
+    err2 = np.abs(from_device(y3) - ref2).max()
+    assert err2 <= tolerance(dtype, ref2), (name, "second input set", err2)
     plan.close()
 
 

@@ -301,6 +301,16 @@ def run_ours(args, wl):
         raise RuntimeError("device status after timing: %s" % cc3d.cc3d_status_string(st))
     ms_per_step = ms / args.steps
     value = wl.flops * world * args.steps / (ms / 1e3) / 1e12
+    # per-step durations (first launch start to last launch end of each step) and algorithmic bytes
+    step_ms = sorted(row[0][0].elapsed_time(row[-1][1]) for row in launch_evs)
+    step_stats = {"min": step_ms[0], "mean": sum(step_ms) / len(step_ms),
+                  "p99": step_ms[min(len(step_ms) - 1, int(round(0.99 * (len(step_ms) - 1))))]}
+    frame_in, frame_out = H * W * wl.Cin * 2, H * W * wl.Cout * 2
+    bytes_per_step = 0
+    for k, (_, c) in enumerate(bounds):
+        bytes_per_step += c * frame_in + c * frame_out * (2 if r is not None else 1)  # x, y (+ residual)
+        bytes_per_step += (2 * frame_in if k else 0) + 2 * frame_in  # history read, history written
+    hbm_gbs = bytes_per_step * world / (ms_per_step / 1e3) / 1e9
     # per-launch durations of the dominant (only) kernel
     launch_ms = [a.elapsed_time(bb) for row in launch_evs for (a, bb) in row]
     full = [ms_ for ms_, (_, c) in zip(launch_ms, bounds * args.steps) if c == max(wl.chunks)]
@@ -383,6 +393,9 @@ def run_ours(args, wl):
                 "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": args.steps * len(bounds) * plan.launches_per_chunk,
         "clocks": clocks.summary(),
+        "step_ms": step_stats,
+        "hbm": {"achieved_gbs": hbm_gbs, "peak_gbs": float(p["hbm_gbs"]), "frac": hbm_gbs / world / float(p["hbm_gbs"]),
+                "algorithmic_bytes_per_step": bytes_per_step},
     }
     print(json.dumps(out), flush=True)
     return 0

@@ -131,9 +131,10 @@ class ClockSampler:
 
 def workload_config(wl):
     return {
-        "workload": "%s: causal conv3d Cin=%d Cout=%d k=3x3x3, T=%d frames in chunks %s with a 2-frame "
+        "workload": "%s: causal conv3d Cin=%d Cout=%d k=%dx%dx%d, T=%d frames in chunks %s with a %d-frame "
                     "cache, H=%d W=%d, batch 1, bias%s" % (
-                        wl.name, wl.Cin, wl.Cout, wl.T, "x".join(str(c) for c in sorted(set(wl.chunks))),
+                        wl.name, wl.Cin, wl.Cout, wl.kt, wl.kh, wl.kw, wl.T,
+                        "x".join(str(c) for c in sorted(set(wl.chunks))), wl.kt - 1,
                         wl.H, wl.W, " + residual" if wl.r is not None else ""),
         "Cin": wl.Cin, "Cout": wl.Cout, "T": wl.T, "H": wl.H, "W": wl.W, "chunks": list(wl.chunks),
         "flop_per_step": wl.flops,
@@ -168,17 +169,18 @@ def oracle_sample(wl, rows, nthreads=None):
         raw = np.concatenate(vals).reshape(shape)
         return synth.bf16_bits_to_f64(raw) if wl.dtype == "bf16" else raw.astype(np.float64)
 
-    hist = gen(synth.TID_X, wl.x, (2, H, W, C), t0 - 2)
+    P = wl.kt - 1
+    hist = gen(synth.TID_X, wl.x, (P, H, W, C), t0 - P) if P > 0 else None
     x = gen(synth.TID_X, wl.x, (1, H, W, C), t0)
     w = synth.bf16_bits_to_f64(native.values_host(wl.seed, synth.TID_W, wl.w,
-                                                  synth.dense_index((wl.Cout, 3, 3, 3, C)), wl.dtype))
+                                                  synth.dense_index((wl.Cout, wl.kt, wl.kh, wl.kw, C)), wl.dtype))
     b = synth.bf16_bits_to_f64(native.values_host(wl.seed, synth.TID_B, wl.b, np.arange(wl.Cout), wl.dtype))
     r = gen(synth.TID_R, wl.r, (1, H, W, wl.Cout), t0) if wl.r is not None else None
     n = nthreads or oracle.default_threads()
     ts = time.perf_counter()
     oracle.conv_chunk(x, w, b, r, hist, nthreads=n)
     dt = time.perf_counter() - ts
-    flops = 2.0 * wl.Cin * wl.Cout * 27 * H * W
+    flops = 2.0 * wl.Cin * wl.Cout * wl.kt * wl.kh * wl.kw * H * W
     return flops, dt, n
 
 
@@ -243,14 +245,14 @@ def run_ours(args, wl):
     dt = torch.bfloat16
     T, H, W = wl.T, wl.H, wl.W
     x = native.fill_device(torch.empty((T, H, W, wl.Cin), dtype=dt, device=dev), wl.seed, synth.TID_X, wl.x)
-    wt = native.fill_device(torch.empty((wl.Cout, 3, 3, 3, wl.Cin), dtype=dt, device=dev), wl.seed,
+    wt = native.fill_device(torch.empty((wl.Cout, wl.kt, wl.kh, wl.kw, wl.Cin), dtype=dt, device=dev), wl.seed,
                             synth.TID_W, wl.w)
     b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device=dev), wl.seed, synth.TID_B, wl.b)
     r = None
     if wl.r is not None:
         r = native.fill_device(torch.empty((T, H, W, wl.Cout), dtype=dt, device=dev), wl.seed, synth.TID_R, wl.r)
     y = torch.empty((T, H, W, wl.Cout), dtype=dt, device=dev)
-    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, H, W, dtype="bf16")
+    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, H, W, wl.kt, wl.kh, wl.kw, dtype="bf16")
     caches = [plan.new_cache(dev), plan.new_cache(dev)]
     stream = torch.cuda.Stream(device=dev)
     bounds = []
@@ -309,7 +311,7 @@ def run_ours(args, wl):
     bytes_per_step = 0
     for k, (_, c) in enumerate(bounds):
         bytes_per_step += c * frame_in + c * frame_out * (2 if r is not None else 1)  # x, y (+ residual)
-        bytes_per_step += (2 * frame_in if k else 0) + 2 * frame_in  # history read, history written
+        bytes_per_step += ((wl.kt - 1) * frame_in if k else 0) + (wl.kt - 1) * frame_in  # history read, written
     hbm_gbs = bytes_per_step * world / (ms_per_step / 1e3) / 1e9
     # per-launch durations of the dominant (only) kernel
     launch_ms = [a.elapsed_time(bb) for row in launch_evs for (a, bb) in row]
@@ -317,8 +319,18 @@ def run_ours(args, wl):
     avg_launch_ms = sum(full) / len(full)
     flop_per_launch = wl.flops / T * max(wl.chunks)
     p, src = peaks()
-    achieved = flop_per_launch / (avg_launch_ms / 1e3) / 1e12
-    peak = float(p["bf16_tflops"])
+    # the bound of the dominant kernel: tensor cores unless its arithmetic intensity (FLOP per
+    # algorithmic byte of a full chunk launch, history in and out included) is below the ridge
+    c_full = max(wl.chunks)
+    bytes_per_launch = (c_full * frame_in + c_full * frame_out * (2 if r is not None else 1)
+                        + 2 * (wl.kt - 1) * frame_in)
+    hbm_bound = flop_per_launch / bytes_per_launch < float(p["bf16_tflops"]) * 1e12 / (float(p["hbm_gbs"]) * 1e9)
+    if hbm_bound:
+        achieved = bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
+        peak = float(p["hbm_gbs"])
+    else:
+        achieved = flop_per_launch / (avg_launch_ms / 1e3) / 1e12
+        peak = float(p["bf16_tflops"])
     traffic = traffic_per_launch(wl.name)
 
     # ---- end to end: pinned host inputs -> device -> chunk loop -> host result, every step
@@ -373,7 +385,8 @@ def run_ours(args, wl):
         dist.destroy_process_group()
     if rank != 0:
         return 0
-    peak_note = "%s MEASURED_PEAKS bf16_tflops (burst, kernel timed alone)" % src
+    peak_note = "%s MEASURED_PEAKS %s" % (src, "hbm_gbs (copy bandwidth)" if hbm_bound else
+                                           "bf16_tflops (burst, kernel timed alone)")
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -383,10 +396,10 @@ def run_ours(args, wl):
         "pct_of_dense_bf16_peak": {"measured_burst": 100 * value / world / float(p["bf16_tflops"]),
                                    "measured_sustained": 100 * value / world / float(p["bf16_tflops_sustained"]),
                                    "spec_2250": 100 * value / world / 2250.0},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
-                     "kernel": plan.kernel, "flop_per_launch": flop_per_launch,
-                     "avg_launch_ms": avg_launch_ms},
+        "roofline": {"bound": "hbm" if hbm_bound else "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s" if hbm_bound else "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peak_note, "kernel": plan.kernel, "flop_per_launch": flop_per_launch,
+                     "algorithmic_bytes_per_launch": bytes_per_launch, "avg_launch_ms": avg_launch_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": wl.flops * world * args.steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -415,14 +428,14 @@ def run_single_chunk(args, wl):
     T = min(4, wl.T)
     x = native.fill_device(torch.empty((T, wl.H, wl.W, wl.Cin), dtype=dt, device="cuda"), wl.seed, synth.TID_X,
                            wl.x)
-    w = native.fill_device(torch.empty((wl.Cout, 3, 3, 3, wl.Cin), dtype=dt, device="cuda"), wl.seed,
+    w = native.fill_device(torch.empty((wl.Cout, wl.kt, wl.kh, wl.kw, wl.Cin), dtype=dt, device="cuda"), wl.seed,
                            synth.TID_W, wl.w)
     b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device="cuda"), wl.seed, synth.TID_B, wl.b)
     r = None
     if wl.r is not None:
         r = native.fill_device(torch.empty((T, wl.H, wl.W, wl.Cout), dtype=dt, device="cuda"), wl.seed,
                                synth.TID_R, wl.r)
-    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, wl.H, wl.W)
+    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
     cin, cout = plan.new_cache(), plan.new_cache()
     y = torch.empty((T, wl.H, wl.W, wl.Cout), dtype=dt, device="cuda")
     for _ in range(args.single_chunk):

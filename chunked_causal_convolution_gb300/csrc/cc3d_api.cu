@@ -200,19 +200,21 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
         if (kt > 4 || kh > 5 || kw > 5) return CC3D_ERR_UNSUPPORTED;
         kind = K_SIMT_F32;
     } else {
-        if (kt != 3 || kh != 3 || kw != 3) return CC3D_ERR_UNSUPPORTED;
+        // tensor cores: kt in 1..3 with a square 3x3 or 1x1 spatial kernel (the decoder's 3x3x3,
+        // MemoryBlock 2x3x3, TemporalGrow 3x1x1 and pointwise 1x1x1 layers)
+        if (kt > 3 || kh != kw || (kh != 1 && kh != 3)) return CC3D_ERR_UNSUPPORTED;
         if (Cin % 16 != 0 || Cin > 1024) return CC3D_ERR_UNSUPPORTED;
         if (!(Cout < 16 || (Cout % 16 == 0 && Cout <= 512))) return CC3D_ERR_UNSUPPORTED;
         CB = (Cin % 32 == 0) ? 32 : 16;
         HeadLaunch hprobe;
         memset(&hprobe, 0, sizeof(hprobe));
-        if (head_configure(1, H, W, Cin, Cout, 1, &hprobe)) {
+        if (kt == 3 && kh == 3 && head_configure(1, H, W, Cin, Cout, 1, &hprobe)) {
             kind = K_TC_BF16_HEAD;  // narrow output: taps stacked into N
         } else {
             TcLaunch probe;
             memset(&probe, 0, sizeof(probe));
-            if (!tc_configure(CB, 1, H, W, Cin, Cout, false, &probe) ||
-                !tc_configure(CB, 1, H, W, Cin, Cout, true, &probe))
+            if (!tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, false, &probe) ||
+                !tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, true, &probe))
                 return CC3D_ERR_UNSUPPORTED;
             kind = Cout < 16 ? K_TC_BF16_NARROW : (probe.pair ? K_TC_BF16_PAIR : K_TC_BF16);
         }
@@ -396,7 +398,7 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     // ---- tensor-core path
     TcLaunch L;
     memset(&L, 0, sizeof(L));
-    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, res != nullptr, &L)) return CC3D_ERR_UNSUPPORTED;
+    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, res != nullptr, &L)) return CC3D_ERR_UNSUPPORTED;
     if (p.fault == 2) return cuda_fail("injected tensor-map encode failure");  // nothing launched
     const CUtensorMapSwizzle sw = p.CB == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : p.CB == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -411,7 +413,7 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cuda_fail("cuTensorMapEncodeTiled (x_chunk)");
-        if (cache_in != nullptr) {
+        if (cache_in != nullptr && P > 0) {
             const cuuint64_t cdims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)P};
             if (g_encode(&L.map_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache_in), cdims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -420,21 +422,23 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
         }
     }
     {
-        // weights [Cout][27][Cin] seen as (ci, co, tap) so one box holds 3 * rb K-major tap tiles
-        const cuuint64_t dims[3] = {(cuuint64_t)p.Cin, (cuuint64_t)p.Cout, 27};
-        const cuuint64_t strides[2] = {(cuuint64_t)27 * p.Cin * 2, (cuuint64_t)p.Cin * 2};
-        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)(L.pair ? L.NT / 2 : L.NT), (cuuint32_t)(3 * L.rb)};
+        // weights [Cout][kt*ks*ks][Cin] seen as (ci, co, tap) so one box holds ks * rb K-major tap tiles
+        const int taps = p.kt * p.kh * p.kw;
+        const cuuint64_t dims[3] = {(cuuint64_t)p.Cin, (cuuint64_t)p.Cout, (cuuint64_t)taps};
+        const cuuint64_t strides[2] = {(cuuint64_t)taps * p.Cin * 2, (cuuint64_t)p.Cin * 2};
+        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)(L.pair ? L.NT / 2 : L.NT),
+                                   (cuuint32_t)(p.kh * L.rb)};
         if (g_encode(&L.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cuda_fail("cuTensorMapEncodeTiled (w)");
     }
-    L.has_cache = cache_in != nullptr;
+    L.has_cache = cache_in != nullptr && P > 0;
     L.bias = b;
     L.res = res;
     L.y = y;
     L.x = x;
-    L.cache_in = cache_in;
+    L.cache_in = P > 0 ? cache_in : nullptr;
     L.cache_out = cache_out;
     L.status = d->status;
     L.wait_ns = p.wait_ns;

@@ -21,13 +21,14 @@ enum : unsigned {
 // pixels are numbered in a "padded flat" order f = h * Sp + j with Sp = S + 2:
 // j = 0 and j = S + 1 are the zero columns left and right of the block, so
 // every spatial tap (dh, dw) of every output position f reads the input at
-// f + (dh - 1) * Sp + (dw - 1) -- a pure shift.  A tile is SUB groups of 128
+// f + (dh - 1) * Sp + (dw - 1) -- a pure shift (1x1 spatial kernels read f itself).  A tile is SUB groups of 128
 // consecutive output positions (one MMA row block each); in row-aligned mode
 // (S == 128) each group is exactly one row segment, otherwise groups are
 // consecutive 128-blocks of f and the positions on padding columns or beyond
 // the last row are computed but not stored.
 struct TcGeometry {
     int S, Sp, ncolblk;
+    int halo;           // (ks - 1) / 2: spatial taps reach this far from the output position
     int row_aligned;
     int sub;            // 128-row groups per tile
     int sub_stride;     // f distance between groups (Sp or 128)
@@ -40,14 +41,15 @@ struct TcLaunch {
     // tensor maps (encoded on the host)
     CUtensorMap map_x;      // x_chunk   [T][H][W][Cin]   box (CB, Sp, nrows, 1)
     CUtensorMap map_cache;  // cache_in  [P][H][W][Cin]   same box (unused if no cache)
-    CUtensorMap map_w;      // w viewed as (Cin, Cout, taps) box (CB, NT, 3 * rb)
+    CUtensorMap map_w;      // w viewed as (Cin, Cout, taps) box (CB, NT, ks * rb)
     int T, H, W, Cin, Cout;
+    int kt, ks;             // temporal extent (1..3) and spatial extent kh = kw (1 or 3)
     int NT, nsplit, acc_stages;
     int ncoblk;                       // output-channel blocks handled by separate tiles
     int na, nb;                       // A / B ring stages
     int prefetch;                     // temporal taps of the next tile warmed in L2 (0..3)
     int issuers;                      // MMA-issuing warps (1 or 2)
-    int rb;                           // kernel rows (of 3 taps) per B stage: 1 or 3
+    int rb;                           // kernel rows (of ks taps) per B stage: 1 or 3 (1 when ks == 1)
     int pair;                         // 1: SM-pair kernel (cta_group::2), weight rows split in two
     int split_n;                      // with 2 issuers: split by N slice (else by 128-row group)
     int a_stage_bytes, b_stage_bytes;
@@ -70,7 +72,7 @@ struct TcLaunch {
 
 // Pick tiles / pipeline depths for a tensor-core launch.  Returns false if the
 // shape has no configuration.
-bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, bool has_residual, TcLaunch* L);
+bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, TcLaunch* L);
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 cudaError_t tc2_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 

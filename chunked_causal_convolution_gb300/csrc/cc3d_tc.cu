@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
     const int nissue = L.issuers;              // MMA-issuing warps (1 or 2)
     const uint32_t acc_cols = (uint32_t)(SUB * nsplit * NT);
     const unsigned long long budget = L.wait_ns;
+    const int KSZ = L.ks;     // spatial kernel extent (kh = kw): 3, or 1 for temporal / pointwise kernels
+    const int P = L.kt - 1;   // history frames in the cache
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             int last_pa[kMaxStages], last_pb[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) last_pa[s] = last_pb[s] = -1;
             const uint32_t a_tx = (uint32_t)(ROWB * Sp * L.g.nrows);
-            const uint32_t b_tx = (uint32_t)(ROWB * NT * 3 * RB);
+            const uint32_t b_tx = (uint32_t)(ROWB * NT * KSZ * RB);
             bool skip_first = (L.fault == 1);
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
@@ -124,19 +126,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                 const int next = tile + (int)gridDim.x;
                 if (L.prefetch && next < ntiles) {
                     const TileCoord n = tile_coord(L, next);
-                    for (int dt = 3 - L.prefetch; dt < 3; ++dt) {
-                        const int tin = n.t + dt - 2;
+                    for (int dt = L.kt > L.prefetch ? L.kt - L.prefetch : 0; dt < L.kt; ++dt) {
+                        const int tin = n.t + dt - P;
                         const bool from_cache = tin < 0 && L.has_cache;
                         for (int cb = 0; cb < ncb; ++cb)
                             tma_prefetch_4d(from_cache ? &L.map_cache : &L.map_x, cb * CB, n.w0 - 1, n.hstart,
-                                            from_cache ? tin + 2 : tin);
+                                            from_cache ? tin + P : tin);
                     }
                 }
-                for (int dt = 0; ok && dt < 3; ++dt) {
-                    const int tin = c.t + dt - 2;
+                for (int dt = 0; ok && dt < L.kt; ++dt) {
+                    const int tin = c.t + dt - P;
                     const CUtensorMap* map = &L.map_x;
                     int tc = tin;
-                    if (tin < 0 && L.has_cache) { map = &L.map_cache; tc = tin + 2; }
+                    if (tin < 0 && L.has_cache) { map = &L.map_cache; tc = tin + P; }
                     for (int cb = 0; ok && cb < ncb; ++cb) {
                         if (!bounded_wait(&a_empty[sa], pa ^ 1, budget, &abort_flag, kLoaderSleepNs)) {
                             if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                         skip_first = false;
                         last_pa[sa] = pa;
                         if (++sa == L.na) { sa = 0; pa ^= 1; }
-                        for (int dg = 0; ok && dg < 3 / RB; ++dg) {
+                        for (int dg = 0; ok && dg < KSZ / RB; ++dg) {
                             for (int ns = 0; ns < nsplit; ++ns) {
                                 if (!bounded_wait(&b_empty[sb], pb ^ 1, budget, &abort_flag, kLoaderSleepNs)) {
                                     if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                                 }
                                 mbar_arrive_expect_tx(&b_full[sb], b_tx);
                                 tma_load_3d(smB + (size_t)sb * L.b_stage_bytes, &L.map_w, &b_full[sb], cb * CB,
-                                            c.co0 + ns * NT, dt * 9 + dg * 3 * RB);
+                                            c.co0 + ns * NT, dt * KSZ * KSZ + dg * RB * KSZ);
                                 last_pb[sb] = pb;
                                 if (++sb == L.nb) { sb = 0; pb ^= 1; }
                             }
@@ -218,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             uint32_t rowu[SUBI];
 #pragma unroll
             for (int m = 0; m < SUBI; ++m)
-                rowu[m] = (uint32_t)(c.f0 + (m0 + m) * L.g.sub_stride - c.hstart * Sp - Sp - 1) * ROWU;
-            for (int dt = 0; ok && dt < 3; ++dt) {
+                rowu[m] = (uint32_t)(c.f0 + (m0 + m) * L.g.sub_stride - c.hstart * Sp - L.g.halo * (Sp + 1)) * ROWU;
+            for (int dt = 0; ok && dt < L.kt; ++dt) {
                 for (int cb = 0; ok && cb < ncb; ++cb) {
                     if (!warp_bounded_wait(&a_full[sa], pa, budget, &abort_flag)) {
                         if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                     }
                     tc_fence_after();
                     const uint64_t a_st = a_desc0 + (uint64_t)(sa * a_inc);
-                    for (int dg = 0; ok && dg < 3 / RB; ++dg) {
+                    for (int dg = 0; ok && dg < KSZ / RB; ++dg) {
                         for (int ns = 0; ns < nsplit; ++ns) {
                             if (!warp_bounded_wait(&b_full[sb], pb, budget, &abort_flag)) {
                                 if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
@@ -246,12 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                                 const bool first_row = (dt | cb | dh) == 0;
 #pragma unroll
                                 for (int dw = 0; dw < 3; ++dw) {
+                                    if (dw >= KSZ) continue;  // 1x1 spatial kernels: the single tap
 #pragma unroll
                                     for (int m = 0; m < SUBI; ++m) {
 #pragma unroll
                                         for (int ks = 0; ks < KSTEPS; ++ks) {
                                             const uint64_t ad = desc_add(a_row, rowu[m] + dw * ROWU + ks * 2);
-                                            const uint64_t bd = desc_add(b_st, (dr * 3 + dw) * b_tap_inc + ks * 2);
+                                            const uint64_t bd = desc_add(b_st, (dr * KSZ + dw) * b_tap_inc + ks * 2);
                                             const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
                                             if (mine && lead)
                                                 umma_bf16_ss(dcol + (uint32_t)m * m_cols, ad, bd, idesc, acc);
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         const int cthreads = nissue == 2 ? 32 : 64;
         const int ctid = threadIdx.x - (nissue == 2 ? 96 : 64);
         const size_t frame_chunks = (size_t)L.H * L.W * L.Cin * 2 / 16;
-        const size_t total = 2 * frame_chunks;
+        const size_t total = (size_t)P * frame_chunks;
         const size_t gthreads = (size_t)gridDim.x * cthreads;
         const uint4* xin = reinterpret_cast<const uint4*>(L.x);
         const uint4* cin = reinterpret_cast<const uint4*>(L.cache_in);
@@ -301,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                     const int j = (int)(i / frame_chunks);
                     const size_t o = i - (size_t)j * frame_chunks;
                     const int src = L.T + j;  // index in the extended stack
-                    if (src >= 2)
-                        v[u] = __ldg(xin + (size_t)(src - 2) * frame_chunks + o);
+                    if (src >= P)
+                        v[u] = __ldg(xin + (size_t)(src - P) * frame_chunks + o);
                     else if (cin != nullptr)
                         v[u] = __ldg(cin + (size_t)src * frame_chunks + o);
                 }
@@ -391,11 +394,14 @@ void* kernel_for(int sub)
 
 }  // namespace
 
-bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, bool has_residual, TcLaunch* L)
+bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, TcLaunch* L)
 {
     (void)has_residual;  // the measured best configuration does not depend on it today
     if (CB != 16 && CB != 32) return false;
     if (Cin % CB != 0) return false;
+    if (kt < 1 || kt > 3 || (ks != 1 && ks != 3)) return false;
+    L->kt = kt;
+    L->ks = ks;
     L->T = T;
     L->H = H;
     L->W = W;
@@ -486,18 +492,20 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, bool has_resid
         g.row_aligned = 0;
     }
     g.Sp = g.S + 2;
+    g.halo = (ks - 1) / 2;
     g.ncolblk = cdiv(W, g.S);
     if (g.row_aligned) {
         g.sub_stride = g.Sp;
         g.tile_f = sub * g.Sp;
         g.tiles_per_cb = cdiv(H, sub);
-        g.nrows = sub + 2;
+        g.nrows = sub + 2 * g.halo;
     } else {
         g.sub_stride = 128;
         g.tile_f = sub * 128;
         g.tiles_per_cb = cdiv(H * g.Sp, g.tile_f);
-        // the last row any view reads is at most 3*Sp + sub*128 past the window start
-        g.nrows = 4 + (sub * 128) / g.Sp;
+        // the reads of a tile span sub*128 positions plus halo*(Sp+1) on each side, which starts
+        // anywhere in the window's first row
+        g.nrows = 2 + 2 * g.halo + (sub * 128) / g.Sp;
     }
     if (g.nrows > 256 || g.Sp > 256) return false;
     // pipeline stages
@@ -507,13 +515,13 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, bool has_resid
     // a B stage holds the taps of `rb` kernel rows (3 or 9 taps) for one N slice: the larger
     // stage amortises the per-stage work of the MMA warps for narrow N with four row groups
     // (measured faster there; with two row groups the deeper 3-tap ring wins)
-    L->rb = (9 * L->NT * rowb <= 64 * 1024 && sub >= 4) ? 3 : 1;
+    L->rb = (ks == 3 && 9 * L->NT * rowb <= 64 * 1024 && sub >= 4) ? 3 : 1;
     L->rb = env_int("CC3D_TC_RB", L->rb);
     if (L->rb != 1 && L->rb != 3) return false;
     const int b_rows = L->pair ? L->NT / 2 : L->NT;  // weight rows of one block
-    if (L->pair) L->rb = env_int("CC3D_TC_RB", 3);
-    if (L->rb != 1 && L->rb != 3) return false;
-    L->b_stage_bytes = (3 * L->rb * b_rows * rowb + 1023) & ~1023;
+    if (L->pair) L->rb = env_int("CC3D_TC_RB", ks == 3 ? 3 : 1);
+    if ((L->rb != 1 && L->rb != 3) || ks % L->rb != 0) return false;
+    L->b_stage_bytes = (ks * L->rb * b_rows * rowb + 1023) & ~1023;
     const int budget = 220 * 1024 - 4 * ntot * L->ncoblk;
     L->na = (L->a_stage_bytes > 40 * 1024) ? 2 : 3;
     L->na = env_int("CC3D_TC_NA", L->na);

@@ -66,6 +66,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int cout_pad = L.ncoblk * nsplit * NT;
     const uint32_t acc_cols = (uint32_t)(SUB * nsplit * NT);
     const unsigned long long budget = L.wait_ns;
+    const int KSZ = L.ks;     // spatial kernel extent (kh = kw): 3, or 1 for temporal / pointwise kernels
+    const int P = L.kt - 1;   // history frames in the cache
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -107,16 +109,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int last_pa[kMaxStages], last_pb[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) last_pa[s] = last_pb[s] = -1;
             const uint32_t a_tx = (uint32_t)(ROWB * Sp * L.g.nrows);
-            const uint32_t b_tx = (uint32_t)(ROWB * NH * 3 * RB);
+            const uint32_t b_tx = (uint32_t)(ROWB * NH * KSZ * RB);
             bool skip_first = (L.fault == 1);
             bool ok = true;
             for (int p = pair0; ok && p < npairs; p += pstride) {
                 const TileCoord c = tile_coord(L, 2 * p + (int)rank);
-                for (int dt = 0; ok && dt < 3; ++dt) {
-                    const int tin = c.t + dt - 2;
+                for (int dt = 0; ok && dt < L.kt; ++dt) {
+                    const int tin = c.t + dt - P;
                     const CUtensorMap* map = &L.map_x;
                     int tc = tin;
-                    if (tin < 0 && L.has_cache) { map = &L.map_cache; tc = tin + 2; }
+                    if (tin < 0 && L.has_cache) { map = &L.map_cache; tc = tin + P; }
                     for (int cb = 0; ok && cb < ncb; ++cb) {
                         if (!bounded_wait(&a_empty[sa], pa ^ 1, budget, &abort_flag)) {
                             if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
@@ -130,7 +132,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         skip_first = false;
                         last_pa[sa] = pa;
                         if (++sa == L.na) { sa = 0; pa ^= 1; }
-                        for (int dg = 0; ok && dg < 3 / RB; ++dg) {
+                        for (int dg = 0; ok && dg < KSZ / RB; ++dg) {
                             for (int ns = 0; ns < nsplit; ++ns) {
                                 if (!bounded_wait(&b_empty[sb], pb ^ 1, budget, &abort_flag)) {
                                     if (!abort_flag) record_failure(L, STATUS_TIMEOUT_LOADER, &abort_flag);
@@ -140,7 +142,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 if (leader) mbar_arrive_expect_tx(&b_full[sb], 2 * b_tx);
                                 tma_load_3d_pair(smB + (size_t)sb * L.b_stage_bytes, &L.map_w,
                                                  mapa_shared(smem_u32(&b_full[sb]), 0), cb * CB,
-                                                 c.co0 + ns * NT + (int)rank * NH, dt * 9 + dg * 3 * RB);
+                                                 c.co0 + ns * NT + (int)rank * NH, dt * KSZ * KSZ + dg * RB * KSZ);
                                 last_pb[sb] = pb;
                                 if (++sb == L.nb) { sb = 0; pb ^= 1; }
                             }
@@ -197,8 +199,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t rowu[SUBI];
 #pragma unroll
             for (int m = 0; m < SUBI; ++m)
-                rowu[m] = (uint32_t)(c.f0 + (m0 + m) * L.g.sub_stride - c.hstart * Sp - Sp - 1) * ROWU;
-            for (int dt = 0; ok && dt < 3; ++dt) {
+                rowu[m] = (uint32_t)(c.f0 + (m0 + m) * L.g.sub_stride - c.hstart * Sp - L.g.halo * (Sp + 1)) * ROWU;
+            for (int dt = 0; ok && dt < L.kt; ++dt) {
                 for (int cb = 0; ok && cb < ncb; ++cb) {
                     if (!warp_bounded_wait(&a_full[sa], pa, budget, &abort_flag)) {
                         if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
@@ -207,7 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint64_t a_st = a_desc0 + (uint64_t)(sa * a_inc);
-                    for (int dg = 0; ok && dg < 3 / RB; ++dg) {
+                    for (int dg = 0; ok && dg < KSZ / RB; ++dg) {
                         for (int ns = 0; ns < nsplit; ++ns) {
                             if (!warp_bounded_wait(&b_full[sb], pb, budget, &abort_flag)) {
                                 if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
@@ -225,12 +227,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 const bool first_row = (dt | cb | dh) == 0;
 #pragma unroll
                                 for (int dw = 0; dw < 3; ++dw) {
+                                    if (dw >= KSZ) continue;  // 1x1 spatial kernels: the single tap
 #pragma unroll
                                     for (int m = 0; m < SUBI; ++m) {
 #pragma unroll
                                         for (int ks = 0; ks < KSTEPS; ++ks) {
                                             const uint64_t ad = desc_add(a_row, rowu[m] + dw * ROWU + ks * 2);
-                                            const uint64_t bd = desc_add(b_st, (dr * 3 + dw) * b_tap_inc + ks * 2);
+                                            const uint64_t bd = desc_add(b_st, (dr * KSZ + dw) * b_tap_inc + ks * 2);
                                             const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
                                             if (mine && lead)
                                                 umma_bf16_ss_pair(dcol + (uint32_t)m * m_cols, ad, bd, idesc, acc);
@@ -258,7 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 3) {
         // ------------------------------------------------------------ temporal cache update
         const size_t frame_chunks = (size_t)L.H * L.W * L.Cin * 2 / 16;
-        const size_t total = 2 * frame_chunks;
+        const size_t total = (size_t)P * frame_chunks;
         const size_t gthreads = (size_t)gridDim.x * 32;
         const uint4* xin = reinterpret_cast<const uint4*>(L.x);
         const uint4* cin = reinterpret_cast<const uint4*>(L.cache_in);
@@ -274,8 +277,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int j = (int)(i / frame_chunks);
                     const size_t o = i - (size_t)j * frame_chunks;
                     const int src = L.T + j;
-                    if (src >= 2)
-                        v[u] = __ldg(xin + (size_t)(src - 2) * frame_chunks + o);
+                    if (src >= P)
+                        v[u] = __ldg(xin + (size_t)(src - P) * frame_chunks + o);
                     else if (cin != nullptr)
                         v[u] = __ldg(cin + (size_t)src * frame_chunks + o);
                 }

@@ -38,7 +38,7 @@ __device__ __forceinline__ TileCoord tile_coord(const TcLaunch& L, int tile)
     const int cbk = r / L.g.tiles_per_cb;
     c.w0 = cbk * L.g.S;
     c.f0 = i * L.g.tile_f + (L.g.row_aligned ? 1 : 0);
-    c.hstart = floor_div(c.f0 - L.g.Sp - 1, L.g.Sp);
+    c.hstart = floor_div(c.f0 - L.g.halo * (L.g.Sp + 1), L.g.Sp);  // padded row of the first input read
     return c;
 }
 

@@ -77,8 +77,12 @@ typedef enum {
  * Create a plan for one layer shape.  Host-only: no CUDA call, no device
  * allocation.  kh and kw must be odd.  Supported in this build:
  *   CC3D_F32  : any Cin, Cout >= 1; 1 <= kt <= 4; kh, kw in {1, 3, 5}.
- *   CC3D_BF16 : kt = kh = kw = 3, Cin a multiple of 16 (<= 1024), Cout a
- *               multiple of 16 (<= 512) or Cout < 16 (narrow output head).
+ *   CC3D_BF16 : 1 <= kt <= 3 and kh = kw in {1, 3} (the decoder's 3x3x3 layers,
+ *               a 2x3x3 MemoryBlock, a 3x1x1 TemporalGrow, 1x1x1 projections);
+ *               Cin a multiple of 16 (<= 1024); Cout a multiple of 16 (<= 512)
+ *               or Cout < 16 (narrow output head).
+ * When kt = 1 there is no history: cache_in is ignored and cache_out may be
+ * NULL.
  * Anything else returns CC3D_ERR_UNSUPPORTED.  On error *out is set to NULL
  * and nothing is leaked.
  */

@@ -221,6 +221,17 @@ WORKLOADS = {
     "sr96": Workload("sr96", 96, 96, 361, 1440, 2560, _chunks(361, 4), "bf16", 5,
                      Dist.normal(1.0), Dist.normal(fan_in_sigma(96)),
                      Dist.uniform(-0.1, 0.1), None),
+    # the decoder's neighbours of the 3x3x3 conv, at the c96 stage's size: a MemoryBlock conv
+    # (kt = 2, one history frame), a TemporalGrow conv (3x1x1) and a pointwise projection (1x1x1)
+    "memblock_c96": Workload("memblock_c96", 96, 96, 24, 360, 640, _chunks(24, 4), "bf16", 7,
+                             Dist.normal(1.0), Dist.normal(fan_in_sigma(96, 2, 3, 3)),
+                             Dist.uniform(-0.1, 0.1), Dist.normal(1.0), kt=2),
+    "temporalgrow_c96": Workload("temporalgrow_c96", 96, 96, 24, 360, 640, _chunks(24, 4), "bf16", 8,
+                                 Dist.normal(1.0), Dist.normal(fan_in_sigma(96, 3, 1, 1)),
+                                 Dist.uniform(-0.1, 0.1), None, kh=1, kw=1),
+    "pointwise_c192": Workload("pointwise_c192", 192, 192, 24, 180, 320, _chunks(24, 4), "bf16", 9,
+                               Dist.normal(1.0), Dist.normal(fan_in_sigma(192, 1, 1, 1)),
+                               Dist.uniform(-0.1, 0.1), None, kt=1, kh=1, kw=1),
     "sr_head3": Workload("sr_head3", 96, 3, 361, 1440, 2560, _chunks(361, 4), "bf16", 6,
                          Dist.normal(1.0), Dist.normal(fan_in_sigma(96)),
                          Dist.uniform(-0.1, 0.1), None),

@@ -31,13 +31,15 @@ def from_device(t) -> np.ndarray:
     return t.to(torch.float64).cpu().numpy()
 
 
-def small_inputs(Cin, Cout, T, H, W, dtype, seed, bias=True, residual=False, x_dist=None):
-    """Dense CPU-generated inputs (raw stored form) for sizes the oracle finishes in seconds."""
+def small_inputs(Cin, Cout, T, H, W, dtype, seed, bias=True, residual=False, x_dist=None, k=(3, 3, 3)):
+    """Dense CPU-generated inputs (raw stored form) for sizes the oracle finishes in seconds;
+    k = (kt, kh, kw) is the kernel extent."""
     e = synth.dense_index
     x_dist = x_dist or synth.Dist.normal(1.0)
     raw = {
         "x": synth.raw(seed, synth.TID_X, x_dist, e((T, H, W, Cin)), dtype),
-        "w": synth.raw(seed, synth.TID_W, synth.Dist.normal(synth.fan_in_sigma(Cin)), e((Cout, 3, 3, 3, Cin)), dtype),
+        "w": synth.raw(seed, synth.TID_W, synth.Dist.normal(synth.fan_in_sigma(Cin, *k)),
+                       e((Cout, k[0], k[1], k[2], Cin)), dtype),
     }
     if bias:
         raw["b"] = synth.raw(seed, synth.TID_B, synth.Dist.uniform(-0.1, 0.1), e((Cout,)), dtype)

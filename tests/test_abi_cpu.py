@@ -51,7 +51,9 @@ def test_status_strings(lib):
     ((16, 16, 8, 8, 3, 3, 3, 7), 1),                 # unknown dtype
     ((24, 16, 8, 8, 3, 3, 3, cc3d.CC3D_BF16), 2),    # Cin not a multiple of 16
     ((32, 24, 8, 8, 3, 3, 3, cc3d.CC3D_BF16), 2),    # Cout >= 16 not a multiple of 16
-    ((32, 32, 8, 8, 2, 3, 3, cc3d.CC3D_BF16), 2),    # bf16 needs 3x3x3 in this build
+    ((32, 32, 8, 8, 3, 5, 5, cc3d.CC3D_BF16), 2),    # bf16: 3x3 or 1x1 spatial kernels only
+    ((32, 32, 8, 8, 3, 3, 1, cc3d.CC3D_BF16), 2),    # bf16: square spatial kernels only
+    ((32, 32, 8, 8, 4, 3, 3, cc3d.CC3D_BF16), 2),    # bf16: temporal extent at most 3
     ((32, 1024, 8, 8, 3, 3, 3, cc3d.CC3D_BF16), 2),  # beyond tensor-memory budget
     ((4, 4, 8, 8, 5, 3, 3, cc3d.CC3D_F32), 2),       # fp32 temporal extent limit
 ])
@@ -67,6 +69,10 @@ def test_plan_create_rejects(lib, args, code):
     ((192, 192, 180, 320, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
     ((384, 384, 90, 160, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
     ((96, 3, 1440, 2560, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_head", 1),
+    ((96, 96, 360, 640, 2, 3, 3, cc3d.CC3D_BF16), "tc_bf16_pair", 1),    # MemoryBlock, 1-frame history
+    ((96, 96, 360, 640, 3, 1, 1, cc3d.CC3D_BF16), "tc_bf16_pair", 1),    # TemporalGrow
+    ((192, 192, 180, 320, 1, 1, 1, cc3d.CC3D_BF16), "tc_bf16", 1),       # pointwise projection
+    ((96, 3, 64, 64, 2, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),     # the narrow head kernel is 3x3x3 only
     ((48, 3, 64, 64, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),   # Cin not a multiple of 32
     ((512, 3, 64, 64, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),  # too wide to stage a row
     ((96, 8, 64, 64, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),   # 9 taps x 8 channels exceed N = 48

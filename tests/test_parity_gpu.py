@@ -64,20 +64,16 @@ SMALL_KERNEL = {
 }
 
 
-def _small_case(name, dtype, Cin, Cout, T, H, W, chunks, bias, residual):
+def _check_small(name, dtype, Cin, Cout, T, H, W, chunks, bias, residual, k=(3, 3, 3), kernel=None):
+    """Element-wise parity with the oracle, history bytes, bit-identity across chunkings, and a
+    second input set right after the first."""
     x_dist = synth.Dist.uniform(-1.0, 1.0) if name == "tiny_f32_workload" else None
     seed = 0 if name == "tiny_f32_workload" else 100 + len(name)
-    raw = small_inputs(Cin, Cout, T, H, W, dtype, seed, bias, residual, x_dist=x_dist)
-    dev = {k: to_device(v, dtype) for k, v in raw.items()}
-    plan = cc3d.CausalConv3dPlan(Cin, Cout, H, W, dtype=dtype)
-    return raw, dev, plan
-
-
-@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
-def test_small_shapes_match_oracle_elementwise(case):
-    name, dtype, Cin, Cout, T, H, W, chunks, bias, residual = case
-    raw, dev, plan = _small_case(*case)
-    assert plan.kernel == SMALL_KERNEL[name]
+    raw = small_inputs(Cin, Cout, T, H, W, dtype, seed, bias, residual, x_dist=x_dist, k=k)
+    dev = {kk: to_device(v, dtype) for kk, v in raw.items()}
+    plan = cc3d.CausalConv3dPlan(Cin, Cout, H, W, *k, dtype=dtype)
+    if kernel is not None:
+        assert plan.kernel == kernel
     y, caches = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), chunks)
     assert plan.status() == 0
     ref = oracle.conv_whole(to_f64(raw["x"], dtype), to_f64(raw["w"], dtype),
@@ -86,13 +82,15 @@ def test_small_shapes_match_oracle_elementwise(case):
     got = from_device(y)
     err = np.abs(got - ref).max()
     assert err <= tolerance(dtype, ref), (name, err, tolerance(dtype, ref))
-    # every cache_out holds the two input frames preceding the next chunk, bit for bit
+    # every cache_out holds the kt-1 input frames preceding the next chunk, bit for bit
+    P = k[0] - 1
     xs = dev["x"]
     end = 0
     for c, cache in zip(chunks, caches):
         end += c
-        for j in range(2):
-            src = end - 2 + j
+        assert cache.shape[0] == P
+        for j in range(P):
+            src = end - P + j
             exp = xs[src] if src >= 0 else torch.zeros_like(xs[0])
             assert torch.equal(cache[j], exp), (name, end, j)
     # bit-identical across chunkings
@@ -101,9 +99,8 @@ def test_small_shapes_match_oracle_elementwise(case):
         assert torch.equal(y2, y), (name, alt)
     # a second input set right after the first: a stage consumed before its copy landed would
     # still hold the first set's data (repeated launches on equal inputs cannot show that)
-    x_dist = synth.Dist.uniform(-1.0, 1.0) if name == "tiny_f32_workload" else None
-    raw2 = small_inputs(Cin, Cout, T, H, W, dtype, 5000 + len(name), bias, residual, x_dist=x_dist)
-    dev2 = {k: to_device(v, dtype) for k, v in raw2.items()}
+    raw2 = small_inputs(Cin, Cout, T, H, W, dtype, 5000 + len(name), bias, residual, x_dist=x_dist, k=k)
+    dev2 = {kk: to_device(v, dtype) for kk, v in raw2.items()}
     y3, _ = run_chunks(plan, dev2["x"], dev2["w"], dev2.get("b"), dev2.get("r"), chunks)
     assert plan.status() == 0
     ref2 = oracle.conv_whole(to_f64(raw2["x"], dtype), to_f64(raw2["w"], dtype),
@@ -112,6 +109,31 @@ def test_small_shapes_match_oracle_elementwise(case):
     err2 = np.abs(from_device(y3) - ref2).max()
     assert err2 <= tolerance(dtype, ref2), (name, "second input set", err2)
     plan.close()
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_shapes_match_oracle_elementwise(case):
+    _check_small(*case, kernel=SMALL_KERNEL[case[0]])
+
+
+# The decoder's neighbours of the 3x3x3 conv: MemoryBlock (kt = 2, one history frame),
+# TemporalGrow (3x1x1), pointwise projections (1x1x1) and spatial-only kernels (kt = 1).
+EXTENTS = [
+    # name, dtype, Cin, Cout, T, H, W, chunks, bias, residual, (kt, kh, kw), kernel family
+    ("bf16_memblock_kt2_pair", "bf16", 96, 96, 5, 4, 256, [2, 3], True, True, (2, 3, 3), "tc_bf16_pair"),
+    ("bf16_memblock_kt2_flat", "bf16", 64, 64, 4, 6, 100, [1, 3], True, False, (2, 3, 3), "tc_bf16"),
+    ("bf16_temporalgrow_pair", "bf16", 96, 96, 5, 3, 128, [3, 2], True, False, (3, 1, 1), "tc_bf16_pair"),
+    ("bf16_temporalgrow_flat", "bf16", 32, 64, 4, 5, 70, [2, 2], False, True, (3, 1, 1), "tc_bf16"),
+    ("bf16_pointwise", "bf16", 64, 128, 3, 4, 90, [1, 2], True, True, (1, 1, 1), "tc_bf16"),
+    ("bf16_spatial_only", "bf16", 32, 32, 2, 5, 40, [1, 1], True, False, (1, 3, 3), "tc_bf16"),
+    ("bf16_kt2_narrow", "bf16", 96, 3, 3, 4, 50, [2, 1], True, True, (2, 3, 3), "tc_bf16_narrow"),
+    ("f32_kt2", "f32", 8, 8, 4, 5, 6, [1, 3], True, True, (2, 3, 3), "simt_f32"),
+]
+
+
+@pytest.mark.parametrize("case", EXTENTS, ids=[c[0] for c in EXTENTS])
+def test_kernel_extents_match_oracle_elementwise(case):
+    _check_small(*case[:10], k=case[10], kernel=case[11])
 
 
 # ---------------------------------------------------------------- full-size workloads

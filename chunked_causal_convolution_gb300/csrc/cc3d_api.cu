@@ -1,6 +1,7 @@
 // cc3d_api.cu -- the C ABI declared in include/cc3d.h: plans, argument checks, tensor-map
 // encoding and kernel dispatch.  Nothing here computes on the host; every step of the
-// convolution runs in the kernels of cc3d_tc.cu, cc3d_tc2.cu, cc3d_head.cu and cc3d_simt.cu.
+// convolution runs in the kernels of cc3d_tc.cu, cc3d_tc2.cu, cc3d_head.cu, cc3d_stream.cu and
+// cc3d_simt.cu.
 #include <cudaTypedefs.h>
 
 #include <cstdint>
@@ -19,7 +20,14 @@ __device__ unsigned g_status_word;
 
 namespace {
 
-enum KernelKind { K_SIMT_F32 = 0, K_TC_BF16 = 1, K_TC_BF16_NARROW = 2, K_TC_BF16_PAIR = 3, K_TC_BF16_HEAD = 4 };
+enum KernelKind {
+    K_SIMT_F32 = 0,
+    K_TC_BF16 = 1,
+    K_TC_BF16_NARROW = 2,
+    K_TC_BF16_PAIR = 3,
+    K_TC_BF16_HEAD = 4,
+    K_TC_BF16_STREAM = 5
+};
 
 constexpr int kMaxDevices = 64;
 
@@ -168,6 +176,58 @@ static cc3d_status head_forward(const cc3d_plan_s& p, const DeviceInfo& d, int T
     return e == cudaSuccess ? CC3D_OK : cuda_fail("narrow-output kernel launch", e);
 }
 
+// Streaming launch for 1x1 spatial kernels: frames seen as (Cin, H*W) matrices.
+static cc3d_status stream_forward(const cc3d_plan_s& p, const DeviceInfo& d, int T, const void* x, const void* w,
+                                  const void* b, const void* res, const void* cache_in, void* cache_out, void* y,
+                                  cudaStream_t stream)
+{
+    StreamLaunch L;
+    memset(&L, 0, sizeof(L));
+    if (!stream_configure(T, p.H, p.W, p.Cin, p.Cout, p.kt, d.sms, &L)) return CC3D_ERR_UNSUPPORTED;
+    if (p.fault == 2) return cuda_fail("injected tensor-map encode failure");  // nothing launched
+    const int P = p.kt - 1;
+    const cuuint64_t HW = (cuuint64_t)p.H * p.W;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint64_t strides[2] = {(cuuint64_t)p.Cin * 2, HW * p.Cin * 2};
+    const cuuint32_t box[3] = {32, 128, 1};
+    const cuuint64_t dims[3] = {(cuuint64_t)p.Cin, HW, (cuuint64_t)T};
+    if (g_encode(&L.map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cuda_fail("cuTensorMapEncodeTiled (x_chunk)");
+    if (P > 0) {
+        const cuuint64_t cdims[3] = {(cuuint64_t)p.Cin, HW, (cuuint64_t)P};
+        if (cache_in != nullptr &&
+            g_encode(&L.map_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache_in), cdims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_fail("cuTensorMapEncodeTiled (cache_in)");
+        if (g_encode(&L.map_cache_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, cache_out, cdims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_fail("cuTensorMapEncodeTiled (cache_out)");
+    }
+    {
+        // weights [Cout][kt][1][1][Cin] seen as (ci, co, dt): one box = all output channels of one tap
+        const cuuint64_t wdims[3] = {(cuuint64_t)p.Cin, (cuuint64_t)p.Cout, (cuuint64_t)p.kt};
+        const cuuint64_t wstrides[2] = {(cuuint64_t)p.kt * p.Cin * 2, (cuuint64_t)p.Cin * 2};
+        const cuuint32_t wbox[3] = {32, (cuuint32_t)p.Cout, 1};
+        if (g_encode(&L.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), wdims, wstrides, wbox, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_fail("cuTensorMapEncodeTiled (w)");
+    }
+    L.has_cache = P > 0 && cache_in != nullptr;
+    L.bias = b;
+    L.res = res;
+    L.y = y;
+    L.status = d.status;
+    L.wait_ns = p.wait_ns;
+    L.fault = p.fault;
+    const cudaError_t e = stream_launch(L, stream);
+    return e == cudaSuccess ? CC3D_OK : cuda_fail("streaming kernel launch", e);
+}
+
 extern "C" {
 
 const char* cc3d_status_string(cc3d_status s)
@@ -208,8 +268,12 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
         CB = (Cin % 32 == 0) ? 32 : 16;
         HeadLaunch hprobe;
         memset(&hprobe, 0, sizeof(hprobe));
+        StreamLaunch sprobe;
+        memset(&sprobe, 0, sizeof(sprobe));
         if (kt == 3 && kh == 3 && head_configure(1, H, W, Cin, Cout, 1, &hprobe)) {
             kind = K_TC_BF16_HEAD;  // narrow output: taps stacked into N
+        } else if (kh == 1 && stream_configure(1, H, W, Cin, Cout, kt, 1, &sprobe)) {
+            kind = K_TC_BF16_STREAM;  // no spatial taps: HBM-bound, streamed
         } else {
             TcLaunch probe;
             memset(&probe, 0, sizeof(probe));
@@ -249,6 +313,7 @@ const char* cc3d_plan_kernel(cc3d_plan_t plan)
     case K_TC_BF16: return "tc_bf16";
     case K_TC_BF16_PAIR: return "tc_bf16_pair";
     case K_TC_BF16_HEAD: return "tc_bf16_head";
+    case K_TC_BF16_STREAM: return "tc_bf16_stream";
     default: return "tc_bf16_narrow";
     }
 }
@@ -394,6 +459,7 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     }
 
     if (p.kind == K_TC_BF16_HEAD) return head_forward(p, *d, T, x, w, b, res, cache_in, cache_out, y, stream);
+    if (p.kind == K_TC_BF16_STREAM) return stream_forward(p, *d, T, x, w, b, res, cache_in, cache_out, y, stream);
 
     // ---- tensor-core path
     TcLaunch L;

@@ -105,6 +105,30 @@ struct HeadLaunch {
 bool head_configure(int T, int H, int W, int Cin, int Cout, int sms, HeadLaunch* L);
 cudaError_t head_launch(const HeadLaunch& L, cudaStream_t stream);
 
+// Streaming kernel for 1x1 spatial kernels (kt x 1 x 1): frames as [H*W][Cin] matrices.
+struct StreamLaunch {
+    CUtensorMap map_x;          // x_chunk   viewed as (Cin, H*W, T)  box (32, 128, 1)
+    CUtensorMap map_cache;      // cache_in  viewed as (Cin, H*W, P)  same box (unused if no cache)
+    CUtensorMap map_w;          // w         viewed as (Cin, Cout, kt)  box (32, Cout, 1)
+    CUtensorMap map_cache_out;  // cache_out viewed as (Cin, H*W, P)  box (32, 128, 1), stored from shared memory
+    int T, H, W, Cin, Cout, kt;
+    int gmax;                   // output frames per unit (tensor-memory slots of Cout columns)
+    int npb;                    // 128-position blocks per frame
+    long long units;            // (frame group, position block) units, dealt out in equal runs
+    int nstages, w_bytes, x_stage_bytes, tmem_cols;
+    int has_cache;
+    const void* bias;           // bf16 [Cout] or null
+    const void* res;            // bf16 [T][H][W][Cout] or null
+    void* y;                    // bf16 [T][H][W][Cout]
+    unsigned* status;
+    unsigned long long wait_ns;
+    int fault;
+    int grid;
+    size_t smem_bytes;
+};
+bool stream_configure(int T, int H, int W, int Cin, int Cout, int kt, int sms, StreamLaunch* L);
+cudaError_t stream_launch(const StreamLaunch& L, cudaStream_t stream);
+
 // fp32 direct kernel (CUDA cores, fixed accumulation order).
 struct SimtLaunch {
     int T, H, W, Cin, Cout, kt, kh, kw;

@@ -70,8 +70,10 @@ def test_plan_create_rejects(lib, args, code):
     ((384, 384, 90, 160, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16", 1),
     ((96, 3, 1440, 2560, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_head", 1),
     ((96, 96, 360, 640, 2, 3, 3, cc3d.CC3D_BF16), "tc_bf16_pair", 1),    # MemoryBlock, 1-frame history
-    ((96, 96, 360, 640, 3, 1, 1, cc3d.CC3D_BF16), "tc_bf16_pair", 1),    # TemporalGrow
-    ((192, 192, 180, 320, 1, 1, 1, cc3d.CC3D_BF16), "tc_bf16", 1),       # pointwise projection
+    ((96, 96, 360, 640, 3, 1, 1, cc3d.CC3D_BF16), "tc_bf16_stream", 1),  # TemporalGrow
+    ((192, 192, 180, 320, 1, 1, 1, cc3d.CC3D_BF16), "tc_bf16_stream", 1), # pointwise projection
+    ((16, 32, 64, 64, 3, 1, 1, cc3d.CC3D_BF16), "tc_bf16", 1),           # 16-channel blocks: tiles
+    ((64, 384, 64, 64, 1, 1, 1, cc3d.CC3D_BF16), "tc_bf16", 1),          # N > 256: tiles
     ((96, 3, 64, 64, 2, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),     # the narrow head kernel is 3x3x3 only
     ((48, 3, 64, 64, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),   # Cin not a multiple of 32
     ((512, 3, 64, 64, 3, 3, 3, cc3d.CC3D_BF16), "tc_bf16_narrow", 1),  # too wide to stage a row

@@ -122,9 +122,12 @@ EXTENTS = [
     # name, dtype, Cin, Cout, T, H, W, chunks, bias, residual, (kt, kh, kw), kernel family
     ("bf16_memblock_kt2_pair", "bf16", 96, 96, 5, 4, 256, [2, 3], True, True, (2, 3, 3), "tc_bf16_pair"),
     ("bf16_memblock_kt2_flat", "bf16", 64, 64, 4, 6, 100, [1, 3], True, False, (2, 3, 3), "tc_bf16"),
-    ("bf16_temporalgrow_pair", "bf16", 96, 96, 5, 3, 128, [3, 2], True, False, (3, 1, 1), "tc_bf16_pair"),
-    ("bf16_temporalgrow_flat", "bf16", 32, 64, 4, 5, 70, [2, 2], False, True, (3, 1, 1), "tc_bf16"),
-    ("bf16_pointwise", "bf16", 64, 128, 3, 4, 90, [1, 2], True, True, (1, 1, 1), "tc_bf16"),
+    ("bf16_temporalgrow_stream", "bf16", 96, 96, 5, 3, 128, [3, 2], True, False, (3, 1, 1), "tc_bf16_stream"),
+    ("bf16_temporalgrow_stream_res", "bf16", 32, 64, 4, 5, 70, [2, 2], False, True, (3, 1, 1), "tc_bf16_stream"),
+    ("bf16_pointwise_stream", "bf16", 64, 128, 3, 4, 90, [1, 2], True, True, (1, 1, 1), "tc_bf16_stream"),
+    ("bf16_kt2_1x1_stream_groups", "bf16", 64, 256, 9, 3, 50, [9], True, False, (2, 1, 1), "tc_bf16_stream"),
+    ("bf16_temporalgrow_tiles", "bf16", 16, 32, 4, 5, 70, [2, 2], True, False, (3, 1, 1), "tc_bf16"),
+    ("bf16_pointwise_tiles_wide", "bf16", 64, 384, 2, 3, 40, [1, 1], True, False, (1, 1, 1), "tc_bf16"),
     ("bf16_spatial_only", "bf16", 32, 32, 2, 5, 40, [1, 1], True, False, (1, 3, 3), "tc_bf16"),
     ("bf16_kt2_narrow", "bf16", 96, 3, 3, 4, 50, [2, 1], True, True, (2, 3, 3), "tc_bf16_narrow"),
     ("f32_kt2", "f32", 8, 8, 4, 5, 6, [1, 3], True, True, (2, 3, 3), "simt_f32"),

@@ -1,0 +1,99 @@
+"""CUDA-graph replay of a chunk's layer sequence through the C ABI.
+
+A chunk of the super-resolution output stage runs two layers: a 3x3x3 conv (with its own
+history) feeding the 3-channel head (with another).  The sequence is captured once per cache
+parity into a CUDA graph over fixed device buffers; a video is then streamed by copying each
+chunk into the input buffer and replaying.  Outputs and histories must be bit-identical to the
+eager chunk loop.
+"""
+import numpy as np
+import pytest
+import torch
+
+import chunked_causal_convolution_gb300 as cc3d
+import oracle
+from tests.helpers import from_device, small_inputs, to_device, to_f64, tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _layers():
+    T, H, W, C = 8, 6, 136, 32
+    a = small_inputs(C, C, T, H, W, "bf16", 71, bias=True, residual=False)
+    h = small_inputs(C, 3, T, H, W, "bf16", 72, bias=True, residual=False)
+    return T, H, W, C, a, h
+
+
+def test_graph_replay_of_a_two_layer_chunk_is_bit_identical():
+    T, H, W, C, a, h = _layers()
+    Tc = 2
+    x = to_device(a["x"], "bf16")
+    w1, b1 = to_device(a["w"], "bf16"), to_device(a["b"], "bf16")
+    w2, b2 = to_device(h["w"], "bf16"), to_device(h["b"], "bf16")
+    conv = cc3d.CausalConv3dPlan(C, C, H, W)
+    head = cc3d.CausalConv3dPlan(C, 3, H, W)
+    assert head.kernel == "tc_bf16_head"
+
+    # eager reference: chunk loop with ping-pong histories for both layers
+    c1 = [conv.new_cache(), conv.new_cache()]
+    c2 = [head.new_cache(), head.new_cache()]
+    ys = []
+    for k in range(T // Tc):
+        xk = x[k * Tc:(k + 1) * Tc]
+        mid = conv.forward_chunk(xk, w1, b1, None, c1[k % 2] if k else None, c1[(k + 1) % 2])
+        ys.append(head.forward_chunk(mid, w2, b2, None, c2[k % 2] if k else None, c2[(k + 1) % 2]))
+    y_eager = torch.cat(ys)
+    torch.cuda.synchronize()
+    assert conv.status() == 0 and head.status() == 0
+
+    # graphs: fixed input / intermediate / output buffers, one graph per cache parity
+    xs = torch.empty((Tc, H, W, C), dtype=torch.bfloat16, device="cuda")
+    mid = torch.empty((Tc, H, W, C), dtype=torch.bfloat16, device="cuda")
+    ys_buf = torch.empty((Tc, H, W, 3), dtype=torch.bfloat16, device="cuda")
+    g1 = [conv.new_cache(), conv.new_cache()]
+    g2 = [head.new_cache(), head.new_cache()]
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for parity in range(2):
+            # warm the calls up outside the capture (first-use device queries happen there)
+            conv.forward_chunk(xs, w1, b1, None, g1[parity], g1[1 - parity], mid, stream=stream)
+            head.forward_chunk(mid, w2, b2, None, g2[parity], g2[1 - parity], ys_buf, stream=stream)
+        stream.synchronize()
+        for parity in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                conv.forward_chunk(xs, w1, b1, None, g1[parity], g1[1 - parity], mid, stream=stream)
+                head.forward_chunk(mid, w2, b2, None, g2[parity], g2[1 - parity], ys_buf, stream=stream)
+            graphs.append(g)
+    # the first chunk starts from zero histories: reset the buffers the parity-0 graph reads
+    conv.reset(g1[0])
+    head.reset(g2[0])
+    outs = []
+    for k in range(T // Tc):
+        xs.copy_(x[k * Tc:(k + 1) * Tc])
+        graphs[k % 2].replay()
+        outs.append(ys_buf.clone())
+    torch.cuda.synchronize()
+    assert conv.status() == 0 and head.status() == 0
+    y_graph = torch.cat(outs)
+    assert torch.equal(y_graph, y_eager)
+    last = (T // Tc) % 2
+    assert torch.equal(g1[last], c1[last]) and torch.equal(g2[last], c2[last])
+
+    # and the eager result itself is the oracle's two-layer composition (bf16 intermediate)
+    mid_ref = oracle.conv_whole(to_f64(a["x"], "bf16"), to_f64(a["w"], "bf16"), to_f64(a["b"], "bf16"))
+    mid_gpu = torch.cat([conv.forward_chunk(x[k * Tc:(k + 1) * Tc], w1, b1, None,
+                                            c1[k % 2] if k else None, c1[(k + 1) % 2]) for k in range(T // Tc)])
+    assert np.abs(from_device(mid_gpu) - mid_ref).max() <= tolerance("bf16", mid_ref)
+    y_ref = oracle.conv_whole(from_device(mid_gpu), to_f64(h["w"], "bf16"), to_f64(h["b"], "bf16"))
+    assert np.abs(from_device(y_eager) - y_ref).max() <= tolerance("bf16", y_ref)
+    conv.close()
+    head.close()

@@ -25,10 +25,11 @@ import threading
 
 __all__ = [
     "CC3D_F32", "CC3D_BF16", "CC3DError", "CausalConv3dPlan",
-    "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_reset", "cc3d_get_status", "cc3d_destroy",
-    "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
+    "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_forward_chunk_u8", "cc3d_reset", "cc3d_get_status",
+    "cc3d_destroy", "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
     "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_last_error_detail", "library_path",
-    "load_library",
+    "load_library", "FrameWriter",
+    "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
     "weights_from_torch_layout", "EXPORTED_SYMBOLS",
 ]
 
@@ -38,13 +39,15 @@ CC3D_BF16 = 1
 STATUS_NAMES = {
     0: "CC3D_OK", 1: "CC3D_ERR_INVALID_ARG", 2: "CC3D_ERR_UNSUPPORTED", 3: "CC3D_ERR_ALIGNMENT",
     4: "CC3D_ERR_ALIAS", 5: "CC3D_ERR_CUDA", 6: "CC3D_ERR_OOM", 7: "CC3D_ERR_DEVICE_TIMEOUT",
-    8: "CC3D_ERR_NOT_DEVICE_MEMORY",
+    8: "CC3D_ERR_NOT_DEVICE_MEMORY", 9: "CC3D_ERR_IO",
 }
 
 EXPORTED_SYMBOLS = (
-    "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_reset", "cc3d_get_status", "cc3d_destroy",
+    "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_forward_chunk_u8", "cc3d_reset", "cc3d_get_status",
+    "cc3d_destroy",
     "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
     "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_last_error_detail",
+    "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -80,6 +83,7 @@ def load_library():
         vp, i, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong
         lib.cc3d_plan_create.argtypes = [i] * 8 + [ctypes.POINTER(vp)]
         lib.cc3d_forward_chunk.argtypes = [vp, i] + [vp] * 8
+        lib.cc3d_forward_chunk_u8.argtypes = [vp, i] + [vp] * 8
         lib.cc3d_reset.argtypes = [vp, vp, vp]
         lib.cc3d_get_status.argtypes = [vp, vp]
         lib.cc3d_destroy.argtypes = [vp]
@@ -91,9 +95,17 @@ def load_library():
         lib.cc3d_plan_launches_per_chunk.argtypes = [vp]
         lib.cc3d_debug_set_wait_budget_ns.argtypes = [vp, u64]
         lib.cc3d_debug_set_fault.argtypes = [vp, i]
+        lib.cc3d_writer_create.argtypes = [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(vp)]
+        lib.cc3d_writer_submit.argtypes = [vp, vp, ctypes.c_size_t, vp, ctypes.POINTER(ctypes.c_longlong)]
+        lib.cc3d_writer_wait_copied.argtypes = [vp, ctypes.c_longlong, vp]
+        lib.cc3d_writer_close.argtypes = [vp, ctypes.POINTER(ctypes.c_longlong)]
+        for f in (lib.cc3d_writer_create, lib.cc3d_writer_submit, lib.cc3d_writer_wait_copied,
+                  lib.cc3d_writer_close):
+            f.restype = i
         lib.cc3d_last_error_detail.argtypes = []
         lib.cc3d_last_error_detail.restype = ctypes.c_char_p
-        for f in (lib.cc3d_plan_create, lib.cc3d_forward_chunk, lib.cc3d_reset, lib.cc3d_get_status,
+        for f in (lib.cc3d_plan_create, lib.cc3d_forward_chunk, lib.cc3d_forward_chunk_u8, lib.cc3d_reset,
+                  lib.cc3d_get_status,
                   lib.cc3d_plan_launches_per_chunk, lib.cc3d_debug_set_wait_budget_ns,
                   lib.cc3d_debug_set_fault):
             f.restype = i
@@ -158,6 +170,56 @@ def cc3d_forward_chunk(plan, T, x, w, b, residual, cache_in, cache_out, y, strea
     _check(load_library().cc3d_forward_chunk(plan, int(T), _addr(x), _addr(w), _addr(b), _addr(residual),
                                              _addr(cache_in), _addr(cache_out), _addr(y), _stream(stream)),
            "cc3d_forward_chunk")
+
+
+def cc3d_forward_chunk_u8(plan, T, x, w, b, residual, cache_in, cache_out, y_u8, stream=None):
+    _check(load_library().cc3d_forward_chunk_u8(plan, int(T), _addr(x), _addr(w), _addr(b), _addr(residual),
+                                                _addr(cache_in), _addr(cache_out), _addr(y_u8), _stream(stream)),
+           "cc3d_forward_chunk_u8")
+
+
+def cc3d_writer_create(path: str, slot_bytes: int):
+    h = ctypes.c_void_p()
+    _check(load_library().cc3d_writer_create(os.fsencode(path), int(slot_bytes), ctypes.byref(h)),
+           "cc3d_writer_create")
+    return h.value
+
+
+def cc3d_writer_submit(writer, src, nbytes, stream=None) -> int:
+    seq = ctypes.c_longlong(-1)
+    _check(load_library().cc3d_writer_submit(writer, _addr(src), int(nbytes), _stream(stream), ctypes.byref(seq)),
+           "cc3d_writer_submit")
+    return seq.value
+
+
+def cc3d_writer_wait_copied(writer, seq, stream=None):
+    _check(load_library().cc3d_writer_wait_copied(writer, int(seq), _stream(stream)), "cc3d_writer_wait_copied")
+
+
+def cc3d_writer_close(writer) -> int:
+    n = ctypes.c_longlong(0)
+    _check(load_library().cc3d_writer_close(writer, ctypes.byref(n)), "cc3d_writer_close")
+    return n.value
+
+
+class FrameWriter:
+    """The C ABI's asynchronous chunk writer: `submit` a device buffer after the chunk that fills it
+    is enqueued; call `wait_copied(seq, stream)` before that buffer is overwritten; `close` writes
+    everything and returns the bytes written."""
+
+    def __init__(self, path, slot_bytes):
+        self.handle = cc3d_writer_create(path, slot_bytes)
+
+    def submit(self, src, nbytes=None, stream=None) -> int:
+        return cc3d_writer_submit(self.handle, src, src.numel() * src.element_size() if nbytes is None else nbytes,
+                                  stream)
+
+    def wait_copied(self, seq, stream=None):
+        cc3d_writer_wait_copied(self.handle, seq, stream)
+
+    def close(self) -> int:
+        h, self.handle = self.handle, None
+        return cc3d_writer_close(h) if h else 0
 
 
 def cc3d_reset(plan, cache, stream=None):
@@ -241,6 +303,15 @@ class CausalConv3dPlan:
         if y is None and T > 0:
             y = torch.empty((T, self.H, self.W, self.Cout), dtype=self.torch_dtype(), device=x.device)
         cc3d_forward_chunk(self.handle, T, x, w, b, residual, cache_in, cache_out, y, stream)
+        return y
+
+    def forward_chunk_u8(self, x, w, b=None, residual=None, cache_in=None, cache_out=None, y=None, stream=None):
+        """Enqueue one chunk of a narrow-output plan with 8-bit pixels out; returns y (uint8)."""
+        import torch
+        T = 0 if x is None else int(x.shape[0])
+        if y is None and T > 0:
+            y = torch.empty((T, self.H, self.W, self.Cout), dtype=torch.uint8, device=x.device)
+        cc3d_forward_chunk_u8(self.handle, T, x, w, b, residual, cache_in, cache_out, y, stream)
         return y
 
     def reset(self, cache, stream=None):

@@ -122,7 +122,7 @@ struct cc3d_plan_s {
 // channel block).
 static cc3d_status head_forward(const cc3d_plan_s& p, const DeviceInfo& d, int T, const void* x, const void* w,
                                 const void* b, const void* res, const void* cache_in, void* cache_out, void* y,
-                                cudaStream_t stream)
+                                cudaStream_t stream, bool out_u8)
 {
     HeadLaunch L;
     memset(&L, 0, sizeof(L));
@@ -169,6 +169,7 @@ static cc3d_status head_forward(const cc3d_plan_s& p, const DeviceInfo& d, int T
     L.x = x;
     L.cache_in = cache_in;
     L.cache_out = cache_out;
+    L.out_u8 = out_u8 ? 1 : 0;
     L.status = d.status;
     L.wait_ns = p.wait_ns;
     L.fault = p.fault;
@@ -242,6 +243,7 @@ const char* cc3d_status_string(cc3d_status s)
     case CC3D_ERR_OOM: return "out of host memory";
     case CC3D_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
     case CC3D_ERR_NOT_DEVICE_MEMORY: return "pointer is not device memory";
+    case CC3D_ERR_IO: return "host file could not be opened or written";
     }
     return "unknown status";
 }
@@ -375,16 +377,20 @@ cc3d_status cc3d_get_status(cc3d_plan_t plan, void* stream)
     return CC3D_OK;
 }
 
-cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b,
-                               const void* res, const void* cache_in, void* cache_out, void* y, void* stream_)
+}  // extern "C"
+
+// Both forward entry points: y in the plan's dtype, or (out_u8, narrow-head plans) 8-bit pixels.
+static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b, const void* res,
+                                const void* cache_in, void* cache_out, void* y, void* stream_, bool out_u8)
 {
     if (plan == nullptr || T < 0) return CC3D_ERR_INVALID_ARG;
     const cc3d_plan_s& p = *plan;
+    if (out_u8 && p.kind != K_TC_BF16_HEAD) return CC3D_ERR_UNSUPPORTED;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     const size_t es = esize(&p);
     const int P = p.kt - 1;
     const size_t frame_in = (size_t)p.H * p.W * p.Cin * es;
-    const size_t frame_out = (size_t)p.H * p.W * p.Cout * es;
+    const size_t frame_out = (size_t)p.H * p.W * p.Cout * (out_u8 ? 1 : es);
     const size_t n_x = (size_t)T * frame_in, n_y = (size_t)T * frame_out;
     const size_t n_cache = (size_t)P * frame_in;
     const size_t n_w = (size_t)p.Cout * p.kt * p.kh * p.kw * p.Cin * es, n_b = (size_t)p.Cout * es;
@@ -402,10 +408,12 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
             if (q != nullptr && !aligned_to(q, 4)) return CC3D_ERR_ALIGNMENT;
     } else {
         const uintptr_t out_align = (p.Cout % 16 == 0) ? 16 : 2;
+        if (out_u8 && res && !aligned_to(res, 2)) return CC3D_ERR_ALIGNMENT;
         const void* a16[] = {x, w, cache_in, cache_out};
         for (const void* q : a16)
             if (q != nullptr && !aligned_to(q, 16)) return CC3D_ERR_ALIGNMENT;
-        if ((y && !aligned_to(y, out_align)) || (res && !aligned_to(res, out_align)) || (b && !aligned_to(b, 2)))
+        if ((y && !out_u8 && !aligned_to(y, out_align)) || (res && !aligned_to(res, out_align)) ||
+            (b && !aligned_to(b, 2)))
             return CC3D_ERR_ALIGNMENT;
     }
     // ---- overlaps: outputs against everything else
@@ -413,8 +421,9 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
         const void* p;
         size_t n;
     };
+    const size_t n_res = (size_t)T * p.H * p.W * p.Cout * es;
     const Span ins[] = {{T > 0 ? x : nullptr, n_x}, {T > 0 ? w : nullptr, n_w}, {T > 0 ? b : nullptr, n_b},
-                        {T > 0 ? res : nullptr, n_y}, {cache_in, n_cache}};
+                        {T > 0 ? res : nullptr, n_res}, {cache_in, n_cache}};
     for (const Span& s : ins) {
         if (T > 0 && overlaps(y, n_y, s.p, s.n)) return CC3D_ERR_ALIAS;
         if (P > 0 && overlaps(cache_out, n_cache, s.p, s.n)) return CC3D_ERR_ALIAS;
@@ -458,7 +467,8 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
         return CC3D_OK;
     }
 
-    if (p.kind == K_TC_BF16_HEAD) return head_forward(p, *d, T, x, w, b, res, cache_in, cache_out, y, stream);
+    if (p.kind == K_TC_BF16_HEAD)
+        return head_forward(p, *d, T, x, w, b, res, cache_in, cache_out, y, stream, out_u8);
     if (p.kind == K_TC_BF16_STREAM) return stream_forward(p, *d, T, x, w, b, res, cache_in, cache_out, y, stream);
 
     // ---- tensor-core path
@@ -518,6 +528,20 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const voi
     }
     const cudaError_t e = tc_launch(p.CB, L, stream);
     return e == cudaSuccess ? CC3D_OK : cuda_fail("tensor-core kernel launch", e);
+}
+
+extern "C" {
+
+cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b,
+                               const void* res, const void* cache_in, void* cache_out, void* y, void* stream)
+{
+    return forward_impl(plan, T, x, w, b, res, cache_in, cache_out, y, stream, false);
+}
+
+cc3d_status cc3d_forward_chunk_u8(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b,
+                                  const void* res, const void* cache_in, void* cache_out, void* y_u8, void* stream)
+{
+    return forward_impl(plan, T, x, w, b, res, cache_in, cache_out, y_u8, stream, true);
 }
 
 }  // extern "C"

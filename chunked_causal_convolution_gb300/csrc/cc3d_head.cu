@@ -84,6 +84,15 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v)
     tmem_ld_wait();
 }
 
+// The 8-bit output of a pixel value: the bf16 result mapped from [-1, 1] to [0, 255] in fp32
+// (add, multiply, round to nearest even, clamp).
+__device__ __forceinline__ uint8_t quant_u8(float o)
+{
+    const float v = __bfloat162float(__float2bfloat16_rn(o));
+    const float t = __fmul_rn(__fadd_rn(v, 1.0f), 127.5f);
+    return (uint8_t)rintf(fminf(fmaxf(t, 0.0f), 255.0f));
+}
+
 template <int COUT>
 __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_constant__ HeadLaunch L)
 {
@@ -320,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
         const int p = q * 32 + lane;
         const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(L.res);
         __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(L.y);
+        uint8_t* yu8 = reinterpret_cast<uint8_t*>(L.y);
+        const bool out_u8 = L.out_u8 != 0;
         float bias[COUT];
 #pragma unroll
         for (int c = 0; c < COUT; ++c) bias[c] = s_bias[c];
@@ -423,7 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
                             P[t][c] = __fadd_rn(Q[t][c], sdh[1][c]);
                             Q[t][c] = sdh[0][c];
                             const float o = __fadd_rn(__fadd_rn(done, bias[c]), rr[c]);
-                            if (store) y[px * COUT + c] = __float2bfloat16_rn(o);
+                            if (store) {
+                                if (out_u8) yu8[px * COUT + c] = quant_u8(o);
+                                else y[px * COUT + c] = __float2bfloat16_rn(o);
+                            }
                         }
                     }
                 }

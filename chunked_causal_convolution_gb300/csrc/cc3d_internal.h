@@ -92,7 +92,8 @@ struct HeadLaunch {
     int has_cache;
     const void* bias;       // bf16 [Cout] or null
     const void* res;        // bf16 [T][H][W][Cout] or null
-    void* y;                // bf16 [T][H][W][Cout]
+    void* y;                // bf16 [T][H][W][Cout], or uint8 when out_u8
+    int out_u8;             // store clamp(round((y + 1) * 127.5), 0, 255) of the bf16 output instead
     const void* x;
     const void* cache_in;
     void* cache_out;

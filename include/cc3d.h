@@ -57,7 +57,8 @@
 extern "C" {
 #endif
 
-typedef struct cc3d_plan_s* cc3d_plan_t; /* opaque, owned by the library */
+typedef struct cc3d_plan_s* cc3d_plan_t;     /* opaque, owned by the library */
+typedef struct cc3d_writer_s* cc3d_writer_t; /* opaque, owned by the library */
 
 typedef enum { CC3D_F32 = 0, CC3D_BF16 = 1 } cc3d_dtype;
 
@@ -70,7 +71,8 @@ typedef enum {
     CC3D_ERR_CUDA = 5,            /* a CUDA runtime call failed                     */
     CC3D_ERR_OOM = 6,             /* host allocation failed                         */
     CC3D_ERR_DEVICE_TIMEOUT = 7,  /* a bounded wait inside a kernel ran out          */
-    CC3D_ERR_NOT_DEVICE_MEMORY = 8 /* a tensor pointer is not device-accessible       */
+    CC3D_ERR_NOT_DEVICE_MEMORY = 8, /* a tensor pointer is not device-accessible      */
+    CC3D_ERR_IO = 9                /* a host file could not be opened or written      */
 } cc3d_status;
 
 /*
@@ -109,6 +111,54 @@ cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T_chunk, const void* x_chun
                                const void* residual_or_null, const void* cache_in, void* cache_out, void* y,
                                void* stream);
 
+/*
+ * The same chunk with 8-bit pixels out, for narrow-output plans (cc3d_plan_kernel
+ * "tc_bf16_head", e.g. the RGB head of a video decoder): the device-side half of an
+ * asynchronous frame output path (AWS / Synthesia, "How Synthesia optimizes
+ * generative AI video inference on Amazon EC2 G7e instances": chunks are copied to
+ * the host and written while the next chunk computes; 8-bit frames halve those
+ * copies).  Every output value is first rounded to bf16 exactly as
+ * cc3d_forward_chunk stores it (v), then
+ *   y_u8 = clamp(round_to_nearest_even((v + 1) * 127.5), 0, 255)
+ * computed in fp32 (one rounding after the add, one after the multiply): decoder
+ * outputs in [-1, 1] map onto [0, 255].
+ *   y_u8  [T_chunk][H][W][Cout] uint8, any alignment; must not overlap any input.
+ * Other arguments, checks and the history are as in cc3d_forward_chunk.  Plans of
+ * any other kernel family return CC3D_ERR_UNSUPPORTED.
+ */
+cc3d_status cc3d_forward_chunk_u8(cc3d_plan_t plan, int T_chunk, const void* x_chunk, const void* w, const void* b,
+                                  const void* residual_or_null, const void* cache_in, void* cache_out, void* y_u8,
+                                  void* stream);
+
+/*
+ * Asynchronous chunk output (the host half of the frame output path of AWS /
+ * Synthesia, "How Synthesia optimizes generative AI video inference on Amazon EC2
+ * G7e instances": a copy stream beside the compute stream, double buffers in device
+ * and pinned host memory with events as barriers, and a worker thread that writes
+ * the host buffers to storage while the next chunk computes).
+ *
+ * cc3d_writer_create: opens (truncates) the file at `path` and allocates two pinned
+ *   host slots of slot_bytes, a copy stream and events; starts the worker thread.
+ * cc3d_writer_submit: once the work already enqueued on compute_stream is done, copy
+ *   `bytes` (<= slot_bytes) from the device buffer `src` into the next pinned slot on
+ *   the copy stream; the worker appends the slot to the file, in submission order.
+ *   Returns at once unless that slot still holds an unwritten chunk (then it waits for
+ *   the worker).  *seq_out (may be NULL) receives the submission's number (0, 1, ...).
+ *   `src` is read asynchronously: before the caller overwrites it, it calls
+ * cc3d_writer_wait_copied(w, seq, stream): `stream` waits (stream-ordered, no host
+ *   block) until the copy of submission `seq` is done.  seq < 0 is a no-op.
+ * cc3d_writer_close: writes everything submitted, stops the worker, frees the writer
+ *   (also on error); *bytes_written (may be NULL) receives the bytes written.
+ * Errors: CC3D_ERR_INVALID_ARG, CC3D_ERR_NOT_DEVICE_MEMORY (src), CC3D_ERR_CUDA,
+ * CC3D_ERR_OOM, CC3D_ERR_IO (open or write failed; reported by the next submit and
+ * by close).  A writer is used from one host thread at a time.
+ */
+cc3d_status cc3d_writer_create(const char* path, size_t slot_bytes, cc3d_writer_t* out);
+cc3d_status cc3d_writer_submit(cc3d_writer_t w, const void* src, size_t bytes, void* compute_stream,
+                               long long* seq_out);
+cc3d_status cc3d_writer_wait_copied(cc3d_writer_t w, long long seq, void* stream);
+cc3d_status cc3d_writer_close(cc3d_writer_t w, long long* bytes_written);
+
 /* Zero a cache buffer ([kt-1][H][W][Cin]) on the stream: the history of a new
  * video.  Stream-ordered, no allocation.  Same alignment rule as cache_out. */
 cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream);
@@ -128,7 +178,9 @@ const char* cc3d_last_error_detail(void);
 const char* cc3d_status_string(cc3d_status s);
 
 /* Name of the kernel family the plan will launch ("tc_bf16", "tc_bf16_pair" -- SM
- * pairs, "tc_bf16_narrow", "simt_f32"); a static string, NULL for a NULL plan. */
+ * pairs, "tc_bf16_head" -- narrow outputs with the spatial taps stacked into N,
+ * "tc_bf16_stream" -- 1x1 spatial kernels, "tc_bf16_narrow", "simt_f32"); a static
+ * string, NULL for a NULL plan. */
 const char* cc3d_plan_kernel(cc3d_plan_t plan);
 
 /* Number of kernel launches one cc3d_forward_chunk call of this plan makes

@@ -127,3 +127,31 @@ def test_binding_raises_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mod, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         mod.cc3d_plan_create(16, 16, 8, 8)
+
+
+def test_u8_output_is_for_narrow_head_plans_only(lib):
+    # checked before any argument or device work: a wide plan is refused outright
+    p = cc3d.cc3d_plan_create(32, 32, 4, 8, 3, 3, 3, cc3d.CC3D_BF16)
+    try:
+        assert lib.cc3d_forward_chunk_u8(p, 1, None, None, None, None, None, None, None, None) == 2
+    finally:
+        cc3d.cc3d_destroy(p)
+    p = cc3d.cc3d_plan_create(96, 3, 16, 200, 3, 3, 3, cc3d.CC3D_BF16)
+    try:
+        assert cc3d.cc3d_plan_kernel(p) == "tc_bf16_head"
+        assert lib.cc3d_forward_chunk_u8(p, 1, None, None, None, None, None, None, None, None) == 1  # missing x
+    finally:
+        cc3d.cc3d_destroy(p)
+
+
+def test_writer_argument_and_file_errors_need_no_device(lib, tmp_path):
+    import ctypes
+    h = ctypes.c_void_p(123)
+    assert lib.cc3d_writer_create(None, 1024, ctypes.byref(h)) == 1 and h.value is None
+    assert lib.cc3d_writer_create(str(tmp_path / "a.bin").encode(), 0, ctypes.byref(h)) == 1
+    # a path that cannot be opened fails before any CUDA work
+    assert lib.cc3d_writer_create(str(tmp_path / "missing_dir" / "a.bin").encode(), 1024, ctypes.byref(h)) == 9
+    assert h.value is None
+    assert lib.cc3d_writer_submit(None, None, 0, None, None) == 1
+    assert lib.cc3d_writer_wait_copied(None, 0, None) == 1
+    assert lib.cc3d_writer_close(None, None) == 1

@@ -1,0 +1,62 @@
+"""8-bit pixel output of the narrow head (the device half of the asynchronous frame output path).
+
+The uint8 result must be exactly the documented quantisation of the bf16 result the same plan
+produces (both from the same accumulation, so the integer decision is taken on the same value),
+and bit-identical across chunkings; the bf16 result itself is pinned to the oracle by the parity
+tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+import chunked_causal_convolution_gb300 as cc3d
+from tests.helpers import run_chunks, small_inputs, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def quant_u8(y_bf16: torch.Tensor) -> np.ndarray:
+    """clamp(rint((v + 1) * 127.5), 0, 255) in fp32 with one rounding per operation."""
+    v = y_bf16.float().cpu().numpy().astype(np.float32)
+    t = (v + np.float32(1.0)) * np.float32(127.5)
+    return np.clip(np.rint(t), 0, 255).astype(np.uint8)
+
+
+def run_chunks_u8(plan, x, w, b, r, chunks):
+    caches = [plan.new_cache(x.device), plan.new_cache(x.device)]
+    ys, s = [], 0
+    for k, c in enumerate(chunks):
+        ys.append(plan.forward_chunk_u8(x[s:s + c], w, b, r[s:s + c] if r is not None else None,
+                                        caches[k % 2] if k else None, caches[(k + 1) % 2]))
+        s += c
+    return torch.cat(ys)
+
+
+@pytest.mark.parametrize("Cin,Cout,T,H,W,chunks,residual", [
+    (96, 3, 5, 6, 130, [2, 3], True),
+    (32, 1, 4, 9, 300, [1, 3], False),
+])
+def test_u8_head_equals_quantised_bf16_output(Cin, Cout, T, H, W, chunks, residual):
+    raw = small_inputs(Cin, Cout, T, H, W, "bf16", 77 + Cout, bias=True, residual=residual)
+    dev = {k: to_device(v, "bf16") for k, v in raw.items()}
+    plan = cc3d.CausalConv3dPlan(Cin, Cout, H, W)
+    assert plan.kernel == "tc_bf16_head"
+    y, _ = run_chunks(plan, dev["x"], dev["w"], dev["b"], dev.get("r"), chunks)
+    yu8 = run_chunks_u8(plan, dev["x"], dev["w"], dev["b"], dev.get("r"), chunks)
+    assert plan.status() == 0
+    assert yu8.dtype == torch.uint8 and yu8.shape == y.shape
+    exp = quant_u8(y)
+    got = yu8.cpu().numpy()
+    assert np.array_equal(got, exp), int((got != exp).sum())
+    # the outputs (about N(0, 1), with the residual N(0, 2)) reach both clamps and the interior
+    assert (exp == 0).any() and (exp == 255).any() and ((exp > 0) & (exp < 255)).mean() > 0.25
+    for alt in ([T], [1] * T):
+        assert torch.equal(run_chunks_u8(plan, dev["x"], dev["w"], dev["b"], dev.get("r"), alt), yu8)
+    plan.close()

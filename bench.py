@@ -447,6 +447,133 @@ def run_single_chunk(args, wl):
     return 0
 
 
+def run_output_pipeline(args, wl):
+    """Auxiliary measurement (one JSON line, not the bench line): a chunk loop of the narrow head
+    with 8-bit frames out, as compute only, with synchronous output (D2H, then the write, then the
+    next chunk) and with the asynchronous chunk writer of the C ABI."""
+    import torch
+
+    import __graft_entry__
+    import chunked_causal_convolution_gb300 as cc3d
+    import synth
+    from synth import native
+
+    __graft_entry__.build()
+    n, Tc, H, W, dt = args.output_chunks, 4, wl.H, wl.W, torch.bfloat16
+    x = native.fill_device(torch.empty((Tc, H, W, wl.Cin), dtype=dt, device="cuda"), wl.seed, synth.TID_X, wl.x)
+    w = native.fill_device(torch.empty((wl.Cout, wl.kt, wl.kh, wl.kw, wl.Cin), dtype=dt, device="cuda"), wl.seed,
+                           synth.TID_W, wl.w)
+    b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device="cuda"), wl.seed, synth.TID_B, wl.b)
+    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, H, W, wl.kt, wl.kh, wl.kw)
+    caches = [plan.new_cache(), plan.new_cache()]
+    ybuf = [torch.empty((Tc, H, W, wl.Cout), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    nbytes = ybuf[0].numel()
+    s = torch.cuda.Stream()
+
+    def chunk(k, buf):
+        # the same 4-frame input every chunk: the histories still ping-pong as in a stream
+        plan.forward_chunk_u8(x, w, b, None, caches[k % 2], caches[(k + 1) % 2], ybuf[buf], stream=s)
+
+    with torch.cuda.stream(s):
+        for k in range(3):
+            chunk(k, 0)
+    s.synchronize()
+    out = {"measurement": "chunk output path", "workload": wl.name, "chunk_frames": Tc, "chunks": n,
+           "bytes_per_chunk": nbytes, "path": args.output_path}
+    t0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        for k in range(n):
+            chunk(k, k % 2)
+    s.synchronize()
+    out["compute_only_ms_per_chunk"] = (time.perf_counter() - t0) * 1e3 / n
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    with open(args.output_path, "wb") as f:
+        t0 = time.perf_counter()
+        with torch.cuda.stream(s):
+            for k in range(n):
+                chunk(k, 0)
+                host.copy_(ybuf[0].view(-1), non_blocking=True)
+                s.synchronize()
+                f.write(host.numpy().tobytes())
+    out["synchronous_ms_per_chunk"] = (time.perf_counter() - t0) * 1e3 / n
+    writer = cc3d.FrameWriter(args.output_path, nbytes)
+    seqs = [-1, -1]
+    t0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        for k in range(n):
+            buf = k % 2
+            writer.wait_copied(seqs[buf], s)
+            chunk(k, buf)
+            seqs[buf] = writer.submit(ybuf[buf], stream=s)
+    out["bytes_written"] = writer.close()
+    s.synchronize()
+    out["asynchronous_ms_per_chunk"] = (time.perf_counter() - t0) * 1e3 / n
+    out["status"] = plan.status(s)
+    print(json.dumps(out), flush=True)
+    return 0 if out["status"] == 0 else 1
+
+
+def run_graph_timing(args, wl):
+    """Auxiliary measurement (one JSON line, not the bench line): the bench step (the workload's
+    chunk loop) launched eagerly and replayed from one captured CUDA graph."""
+    import torch
+
+    import __graft_entry__
+    import chunked_causal_convolution_gb300 as cc3d
+    import synth
+    from synth import native
+
+    __graft_entry__.build()
+    dt = torch.bfloat16
+    x = native.fill_device(torch.empty((wl.T, wl.H, wl.W, wl.Cin), dtype=dt, device="cuda"), wl.seed, synth.TID_X,
+                           wl.x)
+    w = native.fill_device(torch.empty((wl.Cout, wl.kt, wl.kh, wl.kw, wl.Cin), dtype=dt, device="cuda"), wl.seed,
+                           synth.TID_W, wl.w)
+    b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device="cuda"), wl.seed, synth.TID_B, wl.b)
+    r = (native.fill_device(torch.empty((wl.T, wl.H, wl.W, wl.Cout), dtype=dt, device="cuda"), wl.seed,
+                            synth.TID_R, wl.r) if wl.r is not None else None)
+    y = torch.empty((wl.T, wl.H, wl.W, wl.Cout), dtype=dt, device="cuda")
+    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+    caches = [plan.new_cache(), plan.new_cache()]
+    s = torch.cuda.Stream()
+    bounds, t = [], 0
+    for c in wl.chunks:
+        bounds.append((t, c))
+        t += c
+
+    def step():
+        for k, (s0, c) in enumerate(bounds):
+            cc3d.cc3d_forward_chunk(plan.handle, c, x[s0:s0 + c], w, b, r[s0:s0 + c] if r is not None else None,
+                                    caches[k % 2] if k else None, caches[(k + 1) % 2], y[s0:s0 + c], s)
+
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            step()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    out = {"measurement": "eager vs graph replay", "workload": wl.name, "steps": args.steps}
+    for mode in ("eager", "graph", "eager", "graph"):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(args.steps):
+                if mode == "eager":
+                    step()
+                else:
+                    g.replay()
+            e1.record(s)
+        s.synchronize()
+        out.setdefault(mode + "_ms_per_step", []).append(e0.elapsed_time(e1) / args.steps)
+    out["status"] = plan.status(s)
+    print(json.dumps(out), flush=True)
+    return 0 if out["status"] == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,6 +585,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single-chunk", type=int, default=0,
                     help="profiling case: run this many launches of one 4-frame chunk and exit")
+    ap.add_argument("--output-path", default=None,
+                    help="auxiliary: time the chunk output path of a narrow head writing 8-bit frames here")
+    ap.add_argument("--output-chunks", type=int, default=16)
+    ap.add_argument("--graph-timing", action="store_true",
+                    help="auxiliary: time the step eagerly and replayed from a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warm-up raised to 3 steps")
@@ -466,9 +598,13 @@ def main():
     wl = synth.WORKLOADS[args.workload]
     if args.single_chunk:
         return run_single_chunk(args, wl)  # one 4-frame chunk: fits for every workload
+    if args.output_path:
+        return run_output_pipeline(args, wl)  # one 4-frame input chunk
     if wl.T * wl.H * wl.W * max(wl.Cin, wl.Cout) * 2 > 32e9:
         log("%s does not fit resident on one device; it is covered by the streaming parity test" % wl.name)
         return 2
+    if args.graph_timing:
+        return run_graph_timing(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

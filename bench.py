@@ -143,6 +143,20 @@ def workload_config(wl):
     }
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest value of x over all ranks (the job's time is its slowest rank's); x itself
+    when there is one rank.  device is where the reduction tensor lives (cuda for NCCL, cpu for
+    gloo)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- CPU oracle sample
 
 def oracle_sample(wl, rows, nthreads=None):
@@ -293,11 +307,7 @@ def run_ours(args, wl):
         stream.synchronize()
         time.sleep(0.25)
     barrier()
-    ms = start.elapsed_time(end)
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     st = plan.status(stream)
     if st != 0:
         raise RuntimeError("device status after timing: %s" % cc3d.cc3d_status_string(st))
@@ -359,11 +369,7 @@ def run_ours(args, wl):
         e1.record(stream)
     stream.synchronize()
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     if not torch.equal(yh.to(dev), y):
         raise RuntimeError("end-to-end result differs from the device-resident result")
     h2d = x.numel() * 2 + (r.numel() * 2 if r is not None else 0)

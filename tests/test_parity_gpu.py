@@ -210,6 +210,34 @@ def _gather(y, pts):
 FULL = ["c96_residual", "c192", "c384", "c384_to_192"]
 
 
+def _host_tensor(wl, tid, dist, shape):
+    """A tensor of the workload from the host side of the shared generator (never from the device)."""
+    return to_f64(native.values_host(wl.seed, tid, dist, synth.dense_index(shape), wl.dtype), wl.dtype)
+
+
+@pytest.mark.parametrize("name", ["c96_residual", "c192", "c384"])
+def test_full_frame_compare_at_reduced_T(name):
+    """Every output of the full-resolution layer for 8 frames (two 4-frame chunks), against the
+    oracle evaluated on the whole sequence."""
+    wl = synth.WORKLOADS[name]
+    T = 8
+    d = _gpu_inputs(wl, T=T)
+    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, wl.H, wl.W, dtype=wl.dtype)
+    y, _ = run_chunks(plan, d["x"], d["w"], d.get("b"), d.get("r"), [4, 4])
+    assert plan.status() == 0
+    x = _host_tensor(wl, synth.TID_X, wl.x, (T, wl.H, wl.W, wl.Cin))
+    w = _host_tensor(wl, synth.TID_W, wl.w, (wl.Cout, 3, 3, 3, wl.Cin))
+    b = _host_tensor(wl, synth.TID_B, wl.b, (wl.Cout,)) if wl.b is not None else None
+    r = _host_tensor(wl, synth.TID_R, wl.r, (T, wl.H, wl.W, wl.Cout)) if wl.r is not None else None
+    ref = oracle.conv_whole(x, w, b, r)
+    err = np.abs(from_device(y) - ref).max()
+    tol = tolerance(wl.dtype, ref)
+    assert err <= tol, (name, err, tol)
+    y2, _ = run_chunks(plan, d["x"], d["w"], d.get("b"), d.get("r"), [T])
+    assert torch.equal(y2, y)
+    plan.close()
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_workload_sampled(name):
     wl = synth.WORKLOADS[name]

@@ -391,10 +391,29 @@ def test_non_default_stream():
     assert torch.equal(y_s, y_ref)
 
 
-def test_bounded_wait_times_out_and_the_context_survives():
-    """The loader skips its first copy (test hook), the MMA warp's bounded wait runs out, the kernel
-    records a timeout and returns; the next call on the same context is correct."""
-    raw, d, plan = _tiny_bf16()
+# one small plan of every tensor-core kernel family: (Cin, Cout, H, W, (kt, kh, kw), family)
+FAMILIES = [
+    (32, 32, 6, 40, (3, 3, 3), "tc_bf16"),
+    (96, 96, 3, 256, (3, 3, 3), "tc_bf16_pair"),
+    (96, 3, 6, 130, (3, 3, 3), "tc_bf16_head"),
+    (96, 96, 5, 70, (3, 1, 1), "tc_bf16_stream"),
+    (48, 3, 5, 40, (3, 3, 3), "tc_bf16_narrow"),
+]
+
+
+def _family_case(Cin, Cout, H, W, k, family, T=4):
+    raw = small_inputs(Cin, Cout, T, H, W, "bf16", 7, True, True, k=k)
+    d = {kk: to_device(v, "bf16") for kk, v in raw.items()}
+    plan = cc3d.CausalConv3dPlan(Cin, Cout, H, W, *k)
+    assert plan.kernel == family
+    return d, plan
+
+
+@pytest.mark.parametrize("case", FAMILIES, ids=[c[-1] for c in FAMILIES])
+def test_bounded_wait_times_out_and_the_context_survives(case):
+    """The loader skips its first copy (test hook), a bounded wait runs out, the kernel records a
+    timeout and every role leaves; the next call on the same context is correct."""
+    d, plan = _family_case(*case)
     y_ref, _ = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [4])
     plan.set_wait_budget_ns(50_000_000)
     plan.set_fault(1)
@@ -406,15 +425,18 @@ def test_bounded_wait_times_out_and_the_context_survives():
     y2, _ = run_chunks(plan, d["x"], d["w"], d["b"], d["r"], [4])
     assert plan.status() == 0
     assert torch.equal(y2, y_ref)
+    plan.close()
 
 
-def test_injected_host_encode_failure_launches_nothing():
-    raw, d, plan = _tiny_bf16()
+@pytest.mark.parametrize("case", FAMILIES, ids=[c[-1] for c in FAMILIES])
+def test_injected_host_encode_failure_launches_nothing(case):
+    d, plan = _family_case(*case)
     plan.set_fault(2)
-    y = torch.full((4, 6, 40, 32), 9.0, dtype=torch.bfloat16, device="cuda")
+    y = torch.full((4, case[2], case[3], case[1]), 9.0, dtype=torch.bfloat16, device="cuda")
     cout = plan.new_cache()
     with pytest.raises(cc3d.CC3DError) as e:
         plan.forward_chunk(d["x"], d["w"], d["b"], d["r"], None, cout, y)
     assert e.value.code == 5
     torch.cuda.synchronize()
     assert torch.all(y.float() == 9.0)
+    plan.close()

@@ -25,9 +25,10 @@ import threading
 
 __all__ = [
     "CC3D_F32", "CC3D_BF16", "CC3DError", "CausalConv3dPlan",
-    "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_forward_chunk_u8", "cc3d_reset", "cc3d_get_status",
-    "cc3d_destroy", "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
-    "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_last_error_detail", "library_path",
+    "cc3d_plan_create", "cc3d_plan_create_upsample2x", "cc3d_forward_chunk", "cc3d_forward_chunk_u8",
+    "cc3d_reset", "cc3d_get_status", "cc3d_destroy", "cc3d_status_string", "cc3d_plan_kernel",
+    "cc3d_plan_launches_per_chunk", "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault",
+    "cc3d_last_error_detail", "library_path", "Upsample2xConvPlan",
     "load_library", "FrameWriter",
     "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
     "weights_from_torch_layout", "EXPORTED_SYMBOLS",
@@ -43,7 +44,7 @@ STATUS_NAMES = {
 }
 
 EXPORTED_SYMBOLS = (
-    "cc3d_plan_create", "cc3d_forward_chunk", "cc3d_forward_chunk_u8", "cc3d_reset", "cc3d_get_status",
+    "cc3d_plan_create", "cc3d_plan_create_upsample2x", "cc3d_forward_chunk", "cc3d_forward_chunk_u8", "cc3d_reset", "cc3d_get_status",
     "cc3d_destroy",
     "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
     "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_last_error_detail",
@@ -82,6 +83,7 @@ def load_library():
         lib = ctypes.CDLL(path)
         vp, i, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong
         lib.cc3d_plan_create.argtypes = [i] * 8 + [ctypes.POINTER(vp)]
+        lib.cc3d_plan_create_upsample2x.argtypes = [i] * 6 + [ctypes.POINTER(vp)]
         lib.cc3d_forward_chunk.argtypes = [vp, i] + [vp] * 8
         lib.cc3d_forward_chunk_u8.argtypes = [vp, i] + [vp] * 8
         lib.cc3d_reset.argtypes = [vp, vp, vp]
@@ -104,7 +106,7 @@ def load_library():
             f.restype = i
         lib.cc3d_last_error_detail.argtypes = []
         lib.cc3d_last_error_detail.restype = ctypes.c_char_p
-        for f in (lib.cc3d_plan_create, lib.cc3d_forward_chunk, lib.cc3d_forward_chunk_u8, lib.cc3d_reset,
+        for f in (lib.cc3d_plan_create, lib.cc3d_plan_create_upsample2x, lib.cc3d_forward_chunk, lib.cc3d_forward_chunk_u8, lib.cc3d_reset,
                   lib.cc3d_get_status,
                   lib.cc3d_plan_launches_per_chunk, lib.cc3d_debug_set_wait_budget_ns,
                   lib.cc3d_debug_set_fault):
@@ -163,6 +165,14 @@ def cc3d_plan_create(Cin, Cout, H, W, kt=3, kh=3, kw=3, dtype=CC3D_BF16):
     h = ctypes.c_void_p()
     _check(load_library().cc3d_plan_create(int(Cin), int(Cout), int(H), int(W), int(kt), int(kh), int(kw),
                                            _dtype_code(dtype), ctypes.byref(h)), "cc3d_plan_create")
+    return h.value
+
+
+def cc3d_plan_create_upsample2x(Cin, Cout, H, W, kt=3, dtype=CC3D_BF16):
+    h = ctypes.c_void_p()
+    _check(load_library().cc3d_plan_create_upsample2x(int(Cin), int(Cout), int(H), int(W), int(kt),
+                                                      _dtype_code(dtype), ctypes.byref(h)),
+           "cc3d_plan_create_upsample2x")
     return h.value
 
 
@@ -274,6 +284,7 @@ class CausalConv3dPlan:
         self.Cin, self.Cout, self.H, self.W = int(Cin), int(Cout), int(H), int(W)
         self.kt, self.kh, self.kw = int(kt), int(kh), int(kw)
         self.dtype = _dtype_code(dtype)
+        self.Ho, self.Wo = self.H, self.W  # output frame size
         self.handle = cc3d_plan_create(Cin, Cout, H, W, kt, kh, kw, self.dtype)
 
     @property
@@ -301,7 +312,7 @@ class CausalConv3dPlan:
         import torch
         T = 0 if x is None else int(x.shape[0])
         if y is None and T > 0:
-            y = torch.empty((T, self.H, self.W, self.Cout), dtype=self.torch_dtype(), device=x.device)
+            y = torch.empty((T, self.Ho, self.Wo, self.Cout), dtype=self.torch_dtype(), device=x.device)
         cc3d_forward_chunk(self.handle, T, x, w, b, residual, cache_in, cache_out, y, stream)
         return y
 
@@ -310,7 +321,7 @@ class CausalConv3dPlan:
         import torch
         T = 0 if x is None else int(x.shape[0])
         if y is None and T > 0:
-            y = torch.empty((T, self.H, self.W, self.Cout), dtype=torch.uint8, device=x.device)
+            y = torch.empty((T, self.Ho, self.Wo, self.Cout), dtype=torch.uint8, device=x.device)
         cc3d_forward_chunk_u8(self.handle, T, x, w, b, residual, cache_in, cache_out, y, stream)
         return y
 
@@ -336,3 +347,15 @@ class CausalConv3dPlan:
             self.close()
         except Exception:
             pass
+
+
+class Upsample2xConvPlan(CausalConv3dPlan):
+    """A causal kt x 3 x 3 conv reading its H x W input through a fused nearest-2x upsample:
+    outputs (and the residual) are 2H x 2W, histories hold source frames."""
+
+    def __init__(self, Cin, Cout, H, W, kt=3, dtype="bf16"):
+        self.Cin, self.Cout, self.H, self.W = int(Cin), int(Cout), int(H), int(W)
+        self.kt, self.kh, self.kw = int(kt), 3, 3
+        self.dtype = _dtype_code(dtype)
+        self.Ho, self.Wo = 2 * self.H, 2 * self.W
+        self.handle = cc3d_plan_create_upsample2x(Cin, Cout, H, W, kt, self.dtype)

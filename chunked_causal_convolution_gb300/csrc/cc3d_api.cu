@@ -26,7 +26,8 @@ enum KernelKind {
     K_TC_BF16_NARROW = 2,
     K_TC_BF16_PAIR = 3,
     K_TC_BF16_HEAD = 4,
-    K_TC_BF16_STREAM = 5
+    K_TC_BF16_STREAM = 5,
+    K_TC_BF16_UP2 = 6
 };
 
 constexpr int kMaxDevices = 64;
@@ -109,7 +110,8 @@ bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t
 using namespace cc3d;
 
 struct cc3d_plan_s {
-    int Cin, Cout, H, W, kt, kh, kw;
+    int Cin, Cout, H, W, kt, kh, kw;  // H, W: the input frames (an upsampling plan writes 2H x 2W)
+    int up2 = 0;
     cc3d_dtype dtype;
     int kind;
     int CB;
@@ -279,8 +281,8 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
         } else {
             TcLaunch probe;
             memset(&probe, 0, sizeof(probe));
-            if (!tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, false, &probe) ||
-                !tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, true, &probe))
+            if (!tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, false, false, &probe) ||
+                !tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, true, false, &probe))
                 return CC3D_ERR_UNSUPPORTED;
             kind = Cout < 16 ? K_TC_BF16_NARROW : (probe.pair ? K_TC_BF16_PAIR : K_TC_BF16);
         }
@@ -303,6 +305,41 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
     return CC3D_OK;
 }
 
+cc3d_status cc3d_plan_create_upsample2x(int Cin, int Cout, int H, int W, int kt, cc3d_dtype dtype,
+                                        cc3d_plan_t* out)
+{
+    if (out == nullptr) return CC3D_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (Cin < 1 || Cout < 1 || H < 1 || W < 1 || kt < 1) return CC3D_ERR_INVALID_ARG;
+    if (dtype != CC3D_F32 && dtype != CC3D_BF16) return CC3D_ERR_INVALID_ARG;
+    if (dtype != CC3D_BF16 || kt > 3) return CC3D_ERR_UNSUPPORTED;
+    if ((long long)H * W > (1LL << 28) || Cin % 16 != 0 || Cin > 1024 || Cout % 16 != 0 || Cout > 1024)
+        return CC3D_ERR_UNSUPPORTED;
+    const int CB = (Cin % 32 == 0) ? 32 : 16;
+    TcLaunch probe;
+    memset(&probe, 0, sizeof(probe));
+    if (!tc_configure(CB, 1, H, W, Cin, Cout, kt, 3, false, true, &probe) ||
+        !tc_configure(CB, 1, H, W, Cin, Cout, kt, 3, true, true, &probe))
+        return CC3D_ERR_UNSUPPORTED;
+    cc3d_plan_s* p = new (std::nothrow) cc3d_plan_s;
+    if (p == nullptr) return CC3D_ERR_OOM;
+    p->Cin = Cin;
+    p->Cout = Cout;
+    p->H = H;
+    p->W = W;
+    p->kt = kt;
+    p->kh = 3;
+    p->kw = 3;
+    p->up2 = 1;
+    p->dtype = dtype;
+    p->kind = K_TC_BF16_UP2;
+    p->CB = CB;
+    p->wait_ns = 2000000000ull;
+    p->fault = 0;
+    *out = p;
+    return CC3D_OK;
+}
+
 void cc3d_destroy(cc3d_plan_t plan) { delete plan; }
 
 const char* cc3d_last_error_detail(void) { return g_last_detail; }
@@ -316,6 +353,7 @@ const char* cc3d_plan_kernel(cc3d_plan_t plan)
     case K_TC_BF16_PAIR: return "tc_bf16_pair";
     case K_TC_BF16_HEAD: return "tc_bf16_head";
     case K_TC_BF16_STREAM: return "tc_bf16_stream";
+    case K_TC_BF16_UP2: return "tc_bf16_up2";
     default: return "tc_bf16_narrow";
     }
 }
@@ -390,7 +428,9 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
     const size_t es = esize(&p);
     const int P = p.kt - 1;
     const size_t frame_in = (size_t)p.H * p.W * p.Cin * es;
-    const size_t frame_out = (size_t)p.H * p.W * p.Cout * (out_u8 ? 1 : es);
+    // an upsampling plan's outputs (and residual) are 2H x 2W frames
+    const size_t out_px = (size_t)p.H * p.W * (p.up2 ? 4 : 1);
+    const size_t frame_out = out_px * p.Cout * (out_u8 ? 1 : es);
     const size_t n_x = (size_t)T * frame_in, n_y = (size_t)T * frame_out;
     const size_t n_cache = (size_t)P * frame_in;
     const size_t n_w = (size_t)p.Cout * p.kt * p.kh * p.kw * p.Cin * es, n_b = (size_t)p.Cout * es;
@@ -421,7 +461,7 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
         const void* p;
         size_t n;
     };
-    const size_t n_res = (size_t)T * p.H * p.W * p.Cout * es;
+    const size_t n_res = (size_t)T * out_px * p.Cout * es;
     const Span ins[] = {{T > 0 ? x : nullptr, n_x}, {T > 0 ? w : nullptr, n_w}, {T > 0 ? b : nullptr, n_b},
                         {T > 0 ? res : nullptr, n_res}, {cache_in, n_cache}};
     for (const Span& s : ins) {
@@ -474,7 +514,8 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
     // ---- tensor-core path
     TcLaunch L;
     memset(&L, 0, sizeof(L));
-    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, res != nullptr, &L)) return CC3D_ERR_UNSUPPORTED;
+    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, res != nullptr, p.up2 != 0, &L))
+        return CC3D_ERR_UNSUPPORTED;
     if (p.fault == 2) return cuda_fail("injected tensor-map encode failure");  // nothing launched
     const CUtensorMapSwizzle sw = p.CB == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : p.CB == 32 ? CU_TENSOR_MAP_SWIZZLE_64B

@@ -44,6 +44,7 @@ struct TcLaunch {
     CUtensorMap map_w;      // w viewed as (Cin, Cout, taps) box (CB, NT, ks * rb)
     int T, H, W, Cin, Cout;
     int kt, ks;             // temporal extent (1..3) and spatial extent kh = kw (1 or 3)
+    int up2;                // nearest-2x upsampling fused: H x W source frames, 2H x 2W outputs
     int NT, nsplit, acc_stages;
     int ncoblk;                       // output-channel blocks handled by separate tiles
     int na, nb;                       // A / B ring stages
@@ -72,7 +73,8 @@ struct TcLaunch {
 
 // Pick tiles / pipeline depths for a tensor-core launch.  Returns false if the
 // shape has no configuration.
-bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, TcLaunch* L);
+bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, bool up2,
+                  TcLaunch* L);
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 cudaError_t tc2_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
     const int cout_pad = L.ncoblk * nsplit * NT;
     const int SUB = L.g.sub;                   // 128-row groups per tile (all MMA warps together)
     const int nissue = L.issuers;              // MMA-issuing warps (1 or 2)
-    const uint32_t acc_cols = (uint32_t)(SUB * nsplit * NT);
+    const uint32_t acc_cols = (uint32_t)(SUB * nsplit * NT * (L.up2 ? 4 : 1));
     const unsigned long long budget = L.wait_ns;
     const int KSZ = L.ks;     // spatial kernel extent (kh = kw): 3, or 1 for temporal / pointwise kernels
     const int P = L.kt - 1;   // history frames in the cache
@@ -192,8 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         // elect.sync per MMA made the warp reconverge before every instruction and was measured
         // 10 % slower; a lane elected once need not be the polling lane, and that form gave wrong
         // results on first launches.)
-        const bool lead = lane == 0;                                   // issuer index
-        const int m0 = L.split_n ? 0 : k * SUBI;                  // first 128-row group of this warp
+        const bool lead = lane == 0;
+        // first 128-row group of this warp (all of them when the warps split N slices or classes)
+        const int m0 = (L.split_n || L.up2) ? 0 : k * SUBI;
+        // upsampling layers: four output classes per row group, two per MMA warp
+        const int ncls = L.up2 ? 4 : 1;
+        const int cls_lo = L.up2 ? 2 * k : 0, cls_hi = L.up2 ? 2 * k + 2 : 1;
         const int ns_lo = L.split_n ? k : 0, ns_hi = L.split_n ? k + 1 : nsplit;
         const uint32_t idesc = make_idesc_bf16_f32(128, NT);
         const uint64_t a_desc0 = make_sdesc(smem_u32(smA), 16, SBO, LAYOUT, 0);
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         const uint32_t b_inc = (uint32_t)L.b_stage_bytes >> 4;
         const uint32_t b_tap_inc = (uint32_t)NT * ROWU;  // next tap inside a B stage
         const uint32_t row_shift = (uint32_t)Sp * ROWU;  // next padded row inside the A window
-        const uint32_t m_cols = (uint32_t)(nsplit * NT);  // tensor-memory columns per row group
+        const uint32_t m_cols = (uint32_t)(nsplit * NT * ncls);  // tensor-memory columns per row group
         int sa = 0, pa = 0, sb = 0, pb = 0;
         bool ok = true;
         int it = 0;
@@ -241,6 +245,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                             const uint64_t b_st = b_desc0 + (uint64_t)(sb * b_inc);
                             const uint32_t dcol = dbase + (uint32_t)(ns * NT) + (uint32_t)m0 * m_cols;
                             const bool mine = ns >= ns_lo && ns < ns_hi;
+                            if (L.up2) {
+                                // output class (a, b) of source position (i, j) is the upsampled
+                                // pixel (2i + a, 2j + b): its tap (dh, dw) reads source pixel
+                                // (i + floor((a + dh - 1) / 2), j + floor((b + dw - 1) / 2)), a view
+                                // of the same window shifted by 0..2 rows and 0..2 pixels
+                                for (int dr = 0; dr < RB; ++dr) {
+                                    const int dh = dg * RB + dr;
+                                    const bool first_row = (dt | cb | dh) == 0;
+                                    for (int dw = 0; dw < 3; ++dw) {
+                                        for (int cls = cls_lo; cls < cls_hi; ++cls) {
+                                            const int sh1 = ((cls >> 1) + dh + 1) >> 1, sw1 = ((cls & 1) + dw + 1) >> 1;
+                                            const uint64_t view = desc_add(a_st, sh1 * row_shift + sw1 * ROWU);
+                                            const uint32_t dcls = dcol + (uint32_t)(cls * NT);
+#pragma unroll
+                                            for (int m = 0; m < SUBI; ++m) {
+#pragma unroll
+                                                for (int ks = 0; ks < KSTEPS; ++ks) {
+                                                    const uint64_t ad = desc_add(view, rowu[m] + ks * 2);
+                                                    const uint64_t bd = desc_add(b_st, (dr * 3 + dw) * b_tap_inc + ks * 2);
+                                                    const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
+                                                    if (lead) umma_bf16_ss(dcls + (uint32_t)m * m_cols, ad, bd, idesc, acc);
+                                                }
+                                            }
+                                        }
+                                    }
+                                }
+                            } else {
 #pragma unroll
                             for (int dr = 0; dr < RB; ++dr) {
                                 const int dh = dg * RB + dr;
@@ -261,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                                         }
                                     }
                                 }
+                            }
                             }
                             if (lead) umma_commit(&b_empty[sb]);
                             __syncwarp();
@@ -326,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             const int aph = (it / L.acc_stages) & 1;
             const TileCoord c = tile_coord(L, tile);
             // while the accumulators fill, pull this thread's residual lines into L2
-            if (res != nullptr && wide) {
+            if (res != nullptr && wide && !L.up2) {
                 for (int m = 0; m < SUB; ++m) {
                     const int f = c.f0 + m * L.g.sub_stride + q * 32 + lane;
                     const int h = f / Sp;
@@ -354,6 +386,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                 const int jcol = f - h * Sp;
                 const int w = c.w0 + jcol - 1;
                 const bool valid = h < L.H && jcol >= 1 && jcol <= L.g.S && w < L.W;
+                if (L.up2) {
+                    // class (a, b) of source pixel (h, w) is output pixel (2h + a, 2w + b) of the
+                    // 2H x 2W frame
+                    for (int cls = 0; cls < 4; ++cls) {
+                        const size_t oh = valid ? 2 * (size_t)h + (cls >> 1) : 0;
+                        const size_t ow = valid ? 2 * (size_t)w + (cls & 1) : 0;
+                        const size_t px = ((size_t)c.t * 2 * L.H + oh) * 2 * L.W + ow;
+                        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
+                                               (uint32_t)((m * 4 + cls) * NT);
+                        const bool last_slice = (m == SUB - 1) && (cls == 3);
+                        epilogue_slice(tbase, NT, c.co0, px, valid, last_slice, s_bias, L.Cout, wide, res, y,
+                                       [&]() { release_acc(&acc_empty[as], lane); });
+                    }
+                    continue;
+                }
                 const size_t px = ((size_t)c.t * L.H + (valid ? h : 0)) * L.W + (valid ? w : 0);
                 for (int ns = 0; ns < nsplit; ++ns) {
                     const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
@@ -394,7 +441,11 @@ void* kernel_for(int sub)
 
 }  // namespace
 
-bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, TcLaunch* L)
+namespace {
+
+// One attempt at a configuration with at most sub_cap row groups per tile.
+bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, bool up2,
+                         int sub_cap, int smax, TcLaunch* L)
 {
     (void)has_residual;  // the measured best configuration does not depend on it today
     if (CB != 16 && CB != 32) return false;
@@ -407,13 +458,24 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks
     L->W = W;
     L->Cin = Cin;
     L->Cout = Cout;
+    L->up2 = up2 ? 1 : 0;
+    if (up2 && (ks != 3 || Cout % 16 != 0)) return false;
     // output channels per MMA (N) and number of N slices
     // Output channels: NT per MMA, nsplit N slices per tile (they share the input windows), and
     // ncoblk channel blocks handled by different tiles.  Wide layers (more than 256 channels) are
     // cut into channel blocks by default: the tiles then hold two 128-row groups each and load
     // only their block's weights.
     L->ncoblk = 1;
-    if (Cout < 16) {
+    if (up2) {
+        // four output classes per row group share the accumulator budget: channel blocks of at
+        // most 128, each its own tiles
+        int nb = cdiv(Cout, 128);
+        while (nb <= 8 && !(Cout % nb == 0 && (Cout / nb) % 16 == 0)) ++nb;
+        if (nb > 8) return false;
+        L->ncoblk = nb;
+        L->nsplit = 1;
+        L->NT = Cout / nb;
+    } else if (Cout < 16) {
         L->NT = 16;
         L->nsplit = 1;
     } else {
@@ -428,7 +490,7 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks
             L->nsplit = 1;
         }
     }
-    const int ntot = L->NT * L->nsplit;
+    const int ntot = L->NT * L->nsplit * (up2 ? 4 : 1);  // accumulator columns of a row group
     // 128-row groups per tile (sub) and accumulator stages (acc), within the 512 tensor-memory
     // columns (sub * ntot * acc <= 512).  Measured on GB300: more rows per tile share each weight
     // stage and amortise the per-stage work of the MMA warps, which outweighs double-buffering
@@ -450,14 +512,19 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks
     } else {
         return false;
     }
+    if (up2) {
+        sub = ntot <= 128 ? 4 : (ntot <= 256 ? 2 : 1);
+        acc = 1;
+    }
     sub = env_int("CC3D_TC_SUB", sub);
     acc = env_int("CC3D_TC_ACC", acc);
+    if (sub > sub_cap) sub = sub_cap;
     // SM pairs (cta_group::2): both tiles of a pair must use the same window offsets (row-aligned
     // geometry) and the same weights (one output-channel block); then each block holds half of
     // every weight stage and the tensor core reads less shared memory per MMA.  Two row groups
     // per block with double-buffered accumulators, measured best for narrow layers.
     L->pair = 0;
-    if (W % 128 == 0 && L->ncoblk == 1 && L->nsplit == 1 && L->NT >= 32 && L->NT <= 128 &&
+    if (!up2 && W % 128 == 0 && L->ncoblk == 1 && L->nsplit == 1 && L->NT >= 32 && L->NT <= 128 &&
         env_int("CC3D_TC_PAIR", 1)) {
         L->pair = 1;
         sub = env_int("CC3D_TC_SUB", 2);
@@ -469,7 +536,9 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks
     // two MMA warps when the accumulators split evenly: by 128-row groups, else by N slices
     L->issuers = 1;
     L->split_n = 0;
-    if (env_int("CC3D_TC_ISSUERS", 2) == 2) {
+    if (up2) {
+        L->issuers = 2;  // each MMA warp owns two of the four output classes
+    } else if (env_int("CC3D_TC_ISSUERS", 2) == 2) {
         if (sub >= 2) {
             L->issuers = 2;
         } else if (L->nsplit == 2) {
@@ -487,7 +556,7 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks
         g.S = 128;
         g.row_aligned = 1;
     } else {
-        const int nblk = cdiv(W, 254);
+        const int nblk = cdiv(W, smax);
         g.S = cdiv(W, nblk);
         g.row_aligned = 0;
     }
@@ -515,7 +584,7 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks
     // a B stage holds the taps of `rb` kernel rows (3 or 9 taps) for one N slice: the larger
     // stage amortises the per-stage work of the MMA warps for narrow N with four row groups
     // (measured faster there; with two row groups the deeper 3-tap ring wins)
-    L->rb = (ks == 3 && 9 * L->NT * rowb <= 64 * 1024 && sub >= 4) ? 3 : 1;
+    L->rb = (ks == 3 && 9 * L->NT * rowb <= 64 * 1024 && (sub >= 4 || up2)) ? 3 : 1;
     L->rb = env_int("CC3D_TC_RB", L->rb);
     if (L->rb != 1 && L->rb != 3) return false;
     const int b_rows = L->pair ? L->NT / 2 : L->NT;  // weight rows of one block
@@ -534,8 +603,15 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks
         L->na = 2;
         nb = (budget - L->na * L->a_stage_bytes) / L->b_stage_bytes;
         if (nb > kMaxStages) nb = kMaxStages;
-        if (nb < 2) return false;
     }
+    if (nb < 2 && L->rb == 3 && env_int("CC3D_TC_RB", 0) == 0) {
+        // the 9-tap weight stages do not fit beside two windows: 3-tap stages
+        L->rb = 1;
+        L->b_stage_bytes = (ks * b_rows * rowb + 1023) & ~1023;
+        nb = (budget - L->na * L->a_stage_bytes) / L->b_stage_bytes;
+        if (nb > kMaxStages) nb = kMaxStages;
+    }
+    if (nb < 2) return false;
     L->nb = nb;
     // L2 prefetch of the next tile's windows: 0 none, 1..3 = that many temporal taps (newest first);
     // off by default: measured slower on every decoder shape (it competes with the live working set)
@@ -548,10 +624,24 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks
     return true;
 }
 
+}  // namespace
+
+bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, bool up2,
+                  TcLaunch* L)
+{
+    // the preferred tile height and column blocks of up to 254 pixels first; wide flat windows may
+    // need fewer row groups, then narrower column blocks, to leave room for two windows and two
+    // weight stages in shared memory
+    for (int smax : {254, 128})
+        for (int cap = 4; cap >= 1; cap /= 2)
+            if (tc_configure_capped(CB, T, H, W, Cin, Cout, kt, ks, has_residual, up2, cap, smax, L)) return true;
+    return false;
+}
+
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream)
 {
     if (L.pair) return tc2_launch(CB, L, stream);
-    const int subi = (L.issuers == 2 && !L.split_n) ? L.g.sub / 2 : L.g.sub;
+    const int subi = (L.issuers == 2 && !L.split_n && !L.up2) ? L.g.sub / 2 : L.g.sub;
     void* kern = CB == 16 ? (L.rb == 3 ? kernel_for<16, 3>(subi) : kernel_for<16, 1>(subi))
                           : (L.rb == 3 ? kernel_for<32, 3>(subi) : kernel_for<32, 1>(subi));
     if (kern == nullptr) return cudaErrorInvalidValue;

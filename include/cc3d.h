@@ -92,6 +92,22 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
                              cc3d_plan_t* out);
 
 /*
+ * A plan for a causal conv that reads its input through a nearest-2x spatial upsample
+ * (the decoder's upsampling stage: every input pixel becomes a 2x2 block, then a
+ * kt x 3 x 3 conv with zero padding 1), fused so that the 2H x 2W upsampled frames are
+ * never stored:
+ *   y[t, 2h+a, 2w+b, co] = conv(U(x))[...] with U(x)[t, i, j, c] = x[t, i/2, j/2, c].
+ * H and W are the input (source) frames; x_chunk and the histories are [..][H][W][Cin],
+ * y and the residual [T_chunk][2H][2W][Cout].  The history holds the last kt-1 *source*
+ * frames (the upsample is per frame).  The results are bit-identical to a
+ * cc3d_plan_create plan run on the materialised U(x).  bf16 only: Cin and Cout
+ * multiples of 16 (<= 1024), 1 <= kt <= 3; the plan's kernel family is "tc_bf16_up2".
+ * Otherwise as cc3d_plan_create.
+ */
+cc3d_status cc3d_plan_create_upsample2x(int Cin, int Cout, int H, int W, int kt, cc3d_dtype dtype,
+                                        cc3d_plan_t* out);
+
+/*
  * One temporal chunk of T_chunk frames (see the formula above).
  *   x_chunk  [T_chunk][H][W][Cin]  input frames of this chunk.
  *   w, b     weights and bias; b may be NULL (zero bias).
@@ -179,7 +195,8 @@ const char* cc3d_status_string(cc3d_status s);
 
 /* Name of the kernel family the plan will launch ("tc_bf16", "tc_bf16_pair" -- SM
  * pairs, "tc_bf16_head" -- narrow outputs with the spatial taps stacked into N,
- * "tc_bf16_stream" -- 1x1 spatial kernels, "tc_bf16_narrow", "simt_f32"); a static
+ * "tc_bf16_stream" -- 1x1 spatial kernels, "tc_bf16_up2" -- fused nearest-2x
+ * upsampling, "tc_bf16_narrow", "simt_f32"); a static
  * string, NULL for a NULL plan. */
 const char* cc3d_plan_kernel(cc3d_plan_t plan);
 

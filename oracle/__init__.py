@@ -198,3 +198,17 @@ def conv_points(shape, pts, xwin, w, b=None, rpts=None, nthreads=None, _lib=None
                                       _ptr(xwin), _ptr(w), _ptr(b), _ptr(rpts), _ptr(y),
                                       nthreads or default_threads()))
     return y
+
+
+def upsample_nearest2x(x):
+    """Nearest-neighbour 2x spatial upsampling of [T][H][W][C] frames: every input position's
+    features are copied to the 2 x 2 block of output positions it covers ("SwiftVR Inference
+    Optimization" (LightX2V blog), the TemporalGrow section: the nearest-neighbour upsample that
+    feeds the decoder's spatial convolution)."""
+    x = _f64(x)
+    return np.repeat(np.repeat(x, 2, axis=1), 2, axis=2)
+
+
+def conv_upsample2x_whole(x, w, b=None, r=None, nthreads=None, _lib=None):
+    """The convolution of the nearest-2x upsampled sequence: conv_whole(upsample_nearest2x(x))."""
+    return conv_whole(upsample_nearest2x(x), w, b, r, nthreads=nthreads, _lib=_lib)

@@ -155,3 +155,18 @@ def test_writer_argument_and_file_errors_need_no_device(lib, tmp_path):
     assert lib.cc3d_writer_submit(None, None, 0, None, None) == 1
     assert lib.cc3d_writer_wait_copied(None, 0, None) == 1
     assert lib.cc3d_writer_close(None, None) == 1
+
+
+@pytest.mark.parametrize("C", [16, 32, 48, 64, 96, 128, 192, 256, 384, 512])
+def test_every_supported_bf16_shape_gets_a_configuration(lib, C):
+    # channel counts the tensor-core kernels accept, against flat and row-aligned frame widths
+    for Cout in (3, C, 2 * C if 2 * C <= 512 else C // 2):
+        for W in (1, 17, 100, 128, 200, 254, 256, 300, 640, 2560):
+            for H in (1, 8, 1440):
+                p = cc3d.cc3d_plan_create(C, Cout, H, W, 3, 3, 3, cc3d.CC3D_BF16)
+                cc3d.cc3d_destroy(p)
+        for k in ((2, 3, 3), (3, 1, 1), (1, 1, 1)):
+            p = cc3d.cc3d_plan_create(C, C, 64, 100, *k, cc3d.CC3D_BF16)
+            cc3d.cc3d_destroy(p)
+        p = cc3d.cc3d_plan_create_upsample2x(C, C, 32, 100, 3, cc3d.CC3D_BF16)
+        cc3d.cc3d_destroy(p)

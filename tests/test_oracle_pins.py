@@ -271,3 +271,45 @@ def test_rejects_bad_arguments():
         oracle.conv_whole(np.zeros((2, 2, 2, 2)), np.zeros((1, 3, 2, 3, 2)))  # even kh
     with pytest.raises(ValueError):
         oracle.conv_chunked(np.zeros((3, 2, 2, 1)), np.zeros((1, 3, 3, 3, 1)), chunks=[1, 1])
+
+
+# ---------------------------------------------------------------- nearest-2x upsampling (the decoder's
+# upsampling stage feeding a spatial convolution)
+
+def _torch_nearest2x(x):
+    """PyTorch's nearest interpolation, scale (1, 2, 2), on NCDHW (an independent library routine)."""
+    xt = torch.from_numpy(np.ascontiguousarray(x)).permute(3, 0, 1, 2)[None]
+    u = F.interpolate(xt, scale_factor=(1, 2, 2), mode="nearest")
+    return u[0].permute(1, 2, 3, 0).numpy()
+
+
+def test_upsample_matches_library_nearest_interpolation():
+    rng = np.random.default_rng(11)
+    x = rand(rng, 3, 5, 7, 4)
+    u = oracle.upsample_nearest2x(x)
+    assert u.shape == (3, 10, 14, 4)
+    assert np.array_equal(u, _torch_nearest2x(x))
+
+
+@pytest.mark.parametrize("T,H,W,Cin,Cout,kt", [(4, 3, 5, 3, 2, 3), (3, 2, 2, 2, 3, 2), (2, 4, 3, 1, 1, 1)])
+def test_upsample_conv_matches_library_routines(T, H, W, Cin, Cout, kt):
+    rng = np.random.default_rng(T * 100 + H * 10 + W)
+    x, w, b = rand(rng, T, H, W, Cin), rand(rng, Cout, kt, 3, 3, Cin), rand(rng, Cout)
+    r = rand(rng, T, 2 * H, 2 * W, Cout)
+    y = oracle.conv_upsample2x_whole(x, w, b, r)
+    ref = torch_reference(_torch_nearest2x(x), w, b, r)
+    assert y.shape == (T, 2 * H, 2 * W, Cout)
+    assert np.abs(y - ref).max() < 1e-11
+
+
+def test_upsample_conv_of_a_constant_counts_taps_inside_the_upsampled_frame():
+    # x = 1, w = 1: every output counts Cin * min(t+1, kt) * (taps inside the 2H x 2W frame)
+    T, H, W, C = 3, 2, 3, 2
+    y = oracle.conv_upsample2x_whole(np.ones((T, H, W, C)), np.ones((1, 3, 3, 3, C)))
+    Ho, Wo = 2 * H, 2 * W
+    for t in range(T):
+        for h in range(Ho):
+            for w_ in range(Wo):
+                nh = 3 - (h == 0) - (h == Ho - 1)
+                nw = 3 - (w_ == 0) - (w_ == Wo - 1)
+                assert y[t, h, w_, 0] == C * min(t + 1, 3) * nh * nw

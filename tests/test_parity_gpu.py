@@ -49,6 +49,8 @@ SMALL = [
     ("bf16_cb16", "bf16", 16, 32, 4, 9, 17, [1, 1, 2], True, False),
     ("bf16_two_flat_blocks", "bf16", 32, 16, 2, 3, 300, [2], True, False),
     ("bf16_c192_like", "bf16", 192, 192, 3, 8, 64, [2, 1], True, False),
+    ("bf16_c96_wide_flat_window", "bf16", 96, 96, 3, 8, 100, [2, 1], True, True),
+    ("bf16_c256_narrow_column_blocks", "bf16", 256, 256, 2, 3, 254, [1, 1], True, False),
     ("bf16_one_pixel", "bf16", 32, 32, 3, 1, 1, [1, 1, 1], True, True),
 ]
 
@@ -61,6 +63,7 @@ SMALL_KERNEL = {
     "bf16_head_cout1_two_passes": "tc_bf16_head", "bf16_head_cout5_cin256": "tc_bf16_head",
     "bf16_head_cout2": "tc_bf16_head", "bf16_narrow_generic": "tc_bf16_narrow", "bf16_cb16": "tc_bf16",
     "bf16_two_flat_blocks": "tc_bf16", "bf16_c192_like": "tc_bf16", "bf16_one_pixel": "tc_bf16",
+    "bf16_c96_wide_flat_window": "tc_bf16", "bf16_c256_narrow_column_blocks": "tc_bf16",
 }
 
 
@@ -439,4 +442,57 @@ def test_injected_host_encode_failure_launches_nothing(case):
     assert e.value.code == 5
     torch.cuda.synchronize()
     assert torch.all(y.float() == 9.0)
+    plan.close()
+
+
+# ---------------------------------------------------------------- fused nearest-2x upsampling
+
+UP2 = [
+    # name, Cin, Cout, T, H, W (source), chunks, bias, residual, kt
+    ("up2_c64", 64, 64, 4, 5, 33, [2, 2], True, True, 3),
+    ("up2_c96", 96, 96, 3, 4, 50, [1, 2], True, False, 3),
+    ("up2_cout192_blocks", 32, 192, 3, 3, 20, [3], True, True, 3),
+    ("up2_spatial_only", 32, 32, 2, 6, 70, [1, 1], True, False, 1),
+    ("up2_kt2_wide_rows", 32, 64, 3, 2, 128, [2, 1], False, True, 2),
+]
+
+
+@pytest.mark.parametrize("case", UP2, ids=[c[0] for c in UP2])
+def test_upsample_conv_matches_oracle_and_the_materialised_upsample(case):
+    name, Cin, Cout, T, H, W, chunks, bias, residual, kt = case
+    seed = 300 + len(name)
+    raw = small_inputs(Cin, Cout, T, H, W, "bf16", seed, bias, False, k=(kt, 3, 3))
+    if residual:
+        raw["r"] = synth.raw(seed, synth.TID_R, synth.Dist.normal(1.0),
+                             synth.dense_index((T, 2 * H, 2 * W, Cout)), "bf16")
+    dev = {kk: to_device(v, "bf16") for kk, v in raw.items()}
+    plan = cc3d.Upsample2xConvPlan(Cin, Cout, H, W, kt)
+    assert plan.kernel == "tc_bf16_up2"
+    y, caches = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), chunks)
+    assert plan.status() == 0
+    assert y.shape == (T, 2 * H, 2 * W, Cout)
+    ref = oracle.conv_upsample2x_whole(to_f64(raw["x"], "bf16"), to_f64(raw["w"], "bf16"),
+                                       to_f64(raw["b"], "bf16") if bias else None,
+                                       to_f64(raw["r"], "bf16") if residual else None)
+    err = np.abs(from_device(y) - ref).max()
+    assert err <= tolerance("bf16", ref), (name, err)
+    # the history holds the last kt-1 *source* frames
+    end = 0
+    for c, cache in zip(chunks, caches):
+        end += c
+        assert cache.shape == (kt - 1, H, W, Cin)
+        for j in range(kt - 1):
+            src = end - (kt - 1) + j
+            exp = dev["x"][src] if src >= 0 else torch.zeros_like(dev["x"][0])
+            assert torch.equal(cache[j], exp)
+    for alt in ([T], [1] * T):
+        y2, _ = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), alt)
+        assert torch.equal(y2, y), (name, alt)
+    # the same products in the same order as a plain plan on the stored upsampled frames
+    u = dev["x"].repeat_interleave(2, dim=1).repeat_interleave(2, dim=2)
+    plain = cc3d.CausalConv3dPlan(Cin, Cout, 2 * H, 2 * W, kt, 3, 3)
+    y_plain, _ = run_chunks(plain, u, dev["w"], dev.get("b"), dev.get("r"), chunks)
+    assert plain.status() == 0
+    assert torch.equal(y, y_plain), (name, plain.kernel, int((y != y_plain).sum()))
+    plain.close()
     plan.close()

@@ -130,12 +130,15 @@ class ClockSampler:
 
 
 def workload_config(wl):
+    Ho, Wo = wl.out_hw
+    frame = ("H=%d W=%d" % (wl.H, wl.W) if not wl.up2 else
+             "input H=%d W=%d read through a nearest-2x upsample, output H=%d W=%d" % (wl.H, wl.W, Ho, Wo))
     return {
         "workload": "%s: causal conv3d Cin=%d Cout=%d k=%dx%dx%d, T=%d frames in chunks %s with a %d-frame "
-                    "cache, H=%d W=%d, batch 1, bias%s" % (
+                    "cache, %s, batch 1, bias%s" % (
                         wl.name, wl.Cin, wl.Cout, wl.kt, wl.kh, wl.kw, wl.T,
                         "x".join(str(c) for c in sorted(set(wl.chunks))), wl.kt - 1,
-                        wl.H, wl.W, " + residual" if wl.r is not None else ""),
+                        frame, " + residual" if wl.r is not None else ""),
         "Cin": wl.Cin, "Cout": wl.Cout, "T": wl.T, "H": wl.H, "W": wl.W, "chunks": list(wl.chunks),
         "flop_per_step": wl.flops,
         "l2": "inputs larger than L2 (%.2f GB per activation tensor vs 129 MB L2), no flush" % (
@@ -161,7 +164,8 @@ def max_over_ranks(x, dist=None, device="cpu"):
 
 def oracle_sample(wl, rows, nthreads=None):
     """Time the oracle's chunk form on one output frame (first `rows` rows) of the workload, from its
-    2-frame history: returns (metric FLOPs of the outputs computed, seconds, threads)."""
+    2-frame history: returns (metric FLOPs of the outputs computed, seconds, threads).  For an
+    upsampling layer the oracle upsamples rows/2 source rows and convolves the result."""
     import numpy as np
     from concurrent.futures import ThreadPoolExecutor
 
@@ -170,7 +174,7 @@ def oracle_sample(wl, rows, nthreads=None):
     from synth import native
 
     t0 = wl.T // 2
-    H, W, C = rows, wl.W, wl.Cin
+    H, W, C = (rows // 2 if wl.up2 else rows), wl.W, wl.Cin
 
     def gen(tid, dist, shape, frame0):
         # rows 0..rows-1 of frames frame0.. of the global video
@@ -189,12 +193,15 @@ def oracle_sample(wl, rows, nthreads=None):
     w = synth.bf16_bits_to_f64(native.values_host(wl.seed, synth.TID_W, wl.w,
                                                   synth.dense_index((wl.Cout, wl.kt, wl.kh, wl.kw, C)), wl.dtype))
     b = synth.bf16_bits_to_f64(native.values_host(wl.seed, synth.TID_B, wl.b, np.arange(wl.Cout), wl.dtype))
-    r = gen(synth.TID_R, wl.r, (1, H, W, wl.Cout), t0) if wl.r is not None else None
+    r = gen(synth.TID_R, wl.r, (1, H, W, wl.Cout), t0) if wl.r is not None and not wl.up2 else None
     n = nthreads or oracle.default_threads()
     ts = time.perf_counter()
+    if wl.up2:
+        x = oracle.upsample_nearest2x(x)
+        hist = oracle.upsample_nearest2x(hist) if hist is not None else None
     oracle.conv_chunk(x, w, b, r, hist, nthreads=n)
     dt = time.perf_counter() - ts
-    flops = 2.0 * wl.Cin * wl.Cout * wl.kt * wl.kh * wl.kw * H * W
+    flops = 2.0 * wl.Cin * wl.Cout * wl.kt * wl.kh * wl.kw * x.shape[1] * x.shape[2]
     return flops, dt, n
 
 
@@ -258,15 +265,19 @@ def run_ours(args, wl):
     dev = torch.device("cuda", local)
     dt = torch.bfloat16
     T, H, W = wl.T, wl.H, wl.W
+    Ho, Wo = wl.out_hw  # output frames (2H x 2W for an upsampling layer)
     x = native.fill_device(torch.empty((T, H, W, wl.Cin), dtype=dt, device=dev), wl.seed, synth.TID_X, wl.x)
     wt = native.fill_device(torch.empty((wl.Cout, wl.kt, wl.kh, wl.kw, wl.Cin), dtype=dt, device=dev), wl.seed,
                             synth.TID_W, wl.w)
     b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device=dev), wl.seed, synth.TID_B, wl.b)
     r = None
     if wl.r is not None:
-        r = native.fill_device(torch.empty((T, H, W, wl.Cout), dtype=dt, device=dev), wl.seed, synth.TID_R, wl.r)
-    y = torch.empty((T, H, W, wl.Cout), dtype=dt, device=dev)
-    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, H, W, wl.kt, wl.kh, wl.kw, dtype="bf16")
+        r = native.fill_device(torch.empty((T, Ho, Wo, wl.Cout), dtype=dt, device=dev), wl.seed, synth.TID_R, wl.r)
+    y = torch.empty((T, Ho, Wo, wl.Cout), dtype=dt, device=dev)
+    if wl.up2:
+        plan = cc3d.Upsample2xConvPlan(wl.Cin, wl.Cout, H, W, wl.kt, dtype="bf16")
+    else:
+        plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, H, W, wl.kt, wl.kh, wl.kw, dtype="bf16")
     caches = [plan.new_cache(dev), plan.new_cache(dev)]
     stream = torch.cuda.Stream(device=dev)
     bounds = []
@@ -317,7 +328,7 @@ def run_ours(args, wl):
     step_ms = sorted(row[0][0].elapsed_time(row[-1][1]) for row in launch_evs)
     step_stats = {"min": step_ms[0], "mean": sum(step_ms) / len(step_ms),
                   "p99": step_ms[min(len(step_ms) - 1, int(round(0.99 * (len(step_ms) - 1))))]}
-    frame_in, frame_out = H * W * wl.Cin * 2, H * W * wl.Cout * 2
+    frame_in, frame_out = H * W * wl.Cin * 2, Ho * Wo * wl.Cout * 2
     bytes_per_step = 0
     for k, (_, c) in enumerate(bounds):
         bytes_per_step += c * frame_in + c * frame_out * (2 if r is not None else 1)  # x, y (+ residual)
@@ -384,7 +395,7 @@ def run_ours(args, wl):
             flops, secs, reps = flops + f, secs + dt, reps + 1
         cpu = {"value": flops / secs / 1e12, "unit": UNIT, "cores": n, "kind": "oracle",
                "sample": "fp64 oracle chunk form: one whole output frame (frame %d, %dx%d) of %s from its "
-                         "2-frame history, %d times (%.1f s)" % (wl.T // 2, wl.H, wl.W, wl.name, reps, secs)}
+                         "2-frame history, %d times (%.1f s)" % (wl.T // 2, wl.out_hw[0], wl.out_hw[1], wl.name, reps, secs)}
 
     if dist is not None:
         dist.barrier()
@@ -437,13 +448,17 @@ def run_single_chunk(args, wl):
     w = native.fill_device(torch.empty((wl.Cout, wl.kt, wl.kh, wl.kw, wl.Cin), dtype=dt, device="cuda"), wl.seed,
                            synth.TID_W, wl.w)
     b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device="cuda"), wl.seed, synth.TID_B, wl.b)
+    Ho, Wo = wl.out_hw
     r = None
     if wl.r is not None:
-        r = native.fill_device(torch.empty((T, wl.H, wl.W, wl.Cout), dtype=dt, device="cuda"), wl.seed,
+        r = native.fill_device(torch.empty((T, Ho, Wo, wl.Cout), dtype=dt, device="cuda"), wl.seed,
                                synth.TID_R, wl.r)
-    plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+    if wl.up2:
+        plan = cc3d.Upsample2xConvPlan(wl.Cin, wl.Cout, wl.H, wl.W, wl.kt)
+    else:
+        plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
     cin, cout = plan.new_cache(), plan.new_cache()
-    y = torch.empty((T, wl.H, wl.W, wl.Cout), dtype=dt, device="cuda")
+    y = torch.empty((T, Ho, Wo, wl.Cout), dtype=dt, device="cuda")
     for _ in range(args.single_chunk):
         plan.forward_chunk(x, w, b, r, cin, cout, y)
     st = plan.status()
@@ -580,6 +595,80 @@ def run_graph_timing(args, wl):
     return 0 if out["status"] == 0 else 1
 
 
+def run_upsample_compare(args, wl):
+    """Auxiliary measurement (one JSON line, not the bench line): the chunk loop of an upsampling
+    layer with the nearest-2x upsample fused into the conv, against the unfused pipeline that
+    writes each chunk's upsampled frames to memory (a torch broadcast copy) and runs the plain
+    conv plan on them.  The outputs of the two must be bit-identical."""
+    import torch
+
+    import __graft_entry__
+    import chunked_causal_convolution_gb300 as cc3d
+    import synth
+    from synth import native
+
+    if not wl.up2:
+        raise SystemExit("--upsample-compare wants an upsampling workload")
+    __graft_entry__.build()
+    dt = torch.bfloat16
+    Ho, Wo = wl.out_hw
+    x = native.fill_device(torch.empty((wl.T, wl.H, wl.W, wl.Cin), dtype=dt, device="cuda"), wl.seed, synth.TID_X,
+                           wl.x)
+    w = native.fill_device(torch.empty((wl.Cout, wl.kt, wl.kh, wl.kw, wl.Cin), dtype=dt, device="cuda"), wl.seed,
+                           synth.TID_W, wl.w)
+    b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device="cuda"), wl.seed, synth.TID_B, wl.b)
+    fused = cc3d.Upsample2xConvPlan(wl.Cin, wl.Cout, wl.H, wl.W, wl.kt)
+    plain = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, Ho, Wo, wl.kt, 3, 3)
+    fc = [fused.new_cache(), fused.new_cache()]
+    pc = [plain.new_cache(), plain.new_cache()]
+    cmax = max(wl.chunks)
+    xu = torch.empty((cmax, Ho, Wo, wl.Cin), dtype=dt, device="cuda")
+    y_fused = torch.empty((wl.T, Ho, Wo, wl.Cout), dtype=dt, device="cuda")
+    y_plain = torch.empty_like(y_fused)
+    s = torch.cuda.Stream()
+    bounds, t = [], 0
+    for c in wl.chunks:
+        bounds.append((t, c))
+        t += c
+
+    def step_fused():
+        for k, (s0, c) in enumerate(bounds):
+            cc3d.cc3d_forward_chunk(fused.handle, c, x[s0:s0 + c], w, b, None, fc[k % 2] if k else None,
+                                    fc[(k + 1) % 2], y_fused[s0:s0 + c], s)
+
+    def step_plain():
+        for k, (s0, c) in enumerate(bounds):
+            # one broadcast copy: every source position written to its 2 x 2 output block
+            xu[:c].view(c, wl.H, 2, wl.W, 2, wl.Cin).copy_(
+                x[s0:s0 + c, :, None, :, None, :].expand(c, wl.H, 2, wl.W, 2, wl.Cin))
+            cc3d.cc3d_forward_chunk(plain.handle, c, xu[:c], w, b, None, pc[k % 2] if k else None,
+                                    pc[(k + 1) % 2], y_plain[s0:s0 + c], s)
+
+    out = {"measurement": "fused nearest-2x upsample vs upsample written to memory + plain conv",
+           "workload": wl.name, "steps": args.steps, "fused_kernel": fused.kernel, "plain_kernel": plain.kernel,
+           "flop_per_step": wl.flops}
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            step_fused()
+            step_plain()
+    s.synchronize()
+    for mode, fn in (("fused", step_fused), ("unfused", step_plain), ("fused", step_fused), ("unfused", step_plain)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(args.steps):
+                fn()
+            e1.record(s)
+        s.synchronize()
+        out.setdefault(mode + "_ms_per_step", []).append(e0.elapsed_time(e1) / args.steps)
+    out["fused_tflops"] = wl.flops / (min(out["fused_ms_per_step"]) / 1e3) / 1e12
+    out["unfused_tflops"] = wl.flops / (min(out["unfused_ms_per_step"]) / 1e3) / 1e12
+    out["status"] = [fused.status(s), plain.status(s)]
+    out["bit_identical"] = bool(torch.equal(y_fused, y_plain))
+    print(json.dumps(out), flush=True)
+    return 0 if out["status"] == [0, 0] and out["bit_identical"] else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -596,6 +685,8 @@ def main():
     ap.add_argument("--output-chunks", type=int, default=16)
     ap.add_argument("--graph-timing", action="store_true",
                     help="auxiliary: time the step eagerly and replayed from a CUDA graph")
+    ap.add_argument("--upsample-compare", action="store_true",
+                    help="auxiliary: time an upsampling workload fused and with the upsample written to memory")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warm-up raised to 3 steps")
@@ -611,6 +702,8 @@ def main():
         return 2
     if args.graph_timing:
         return run_graph_timing(args, wl)
+    if args.upsample_compare:
+        return run_upsample_compare(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

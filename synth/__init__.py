@@ -191,10 +191,16 @@ class Workload:
     kt: int = 3
     kh: int = 3
     kw: int = 3
+    up2: bool = False  # the conv reads its H x W input through a nearest-2x upsample (2H x 2W outputs)
+
+    @property
+    def out_hw(self):
+        return (2 * self.H, 2 * self.W) if self.up2 else (self.H, self.W)
 
     @property
     def flops(self) -> float:
-        return 2.0 * self.Cin * self.Cout * self.kt * self.kh * self.kw * self.T * self.H * self.W
+        Ho, Wo = self.out_hw
+        return 2.0 * self.Cin * self.Cout * self.kt * self.kh * self.kw * self.T * Ho * Wo
 
 
 def _chunks(T, n):
@@ -232,6 +238,10 @@ WORKLOADS = {
     "pointwise_c192": Workload("pointwise_c192", 192, 192, 24, 180, 320, _chunks(24, 4), "bf16", 9,
                                Dist.normal(1.0), Dist.normal(fan_in_sigma(192, 1, 1, 1)),
                                Dist.uniform(-0.1, 0.1), None, kt=1, kh=1, kw=1),
+    # the decoder's upsampling stage at the c96 stage's output size: 180x320 source frames read
+    # through a nearest-2x upsample by a 96 -> 96 3x3x3 conv producing 360x640 frames
+    "up2_c96": Workload("up2_c96", 96, 96, 24, 180, 320, _chunks(24, 4), "bf16", 10,
+                        Dist.normal(1.0), Dist.normal(fan_in_sigma(96)), Dist.uniform(-0.1, 0.1), None, up2=True),
     "sr_head3": Workload("sr_head3", 96, 3, 361, 1440, 2560, _chunks(361, 4), "bf16", 6,
                          Dist.normal(1.0), Dist.normal(fan_in_sigma(96)),
                          Dist.uniform(-0.1, 0.1), None),

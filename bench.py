@@ -34,7 +34,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tc_bf16_kernel_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "chunked_causal_convolution_gb300", "csrc", f)
-                  for f in ("cc3d_tc.cu", "cc3d_tc2.cu", "cc3d_tc_common.cuh", "cc3d_ptx.cuh")]
+                  for f in ("cc3d_tc.cu", "cc3d_tc2.cu", "cc3d_tc2s.cu", "cc3d_tc_common.cuh", "cc3d_ptx.cuh")]
 
 
 def log(*a):

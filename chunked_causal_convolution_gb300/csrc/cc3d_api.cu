@@ -549,6 +549,14 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cuda_fail("cuTensorMapEncodeTiled (w)");
+        if (L.tstack) {
+            // the two-frame schedule's stacked stages: all NT rows of rb tap rows per block
+            const cuuint32_t box2[3] = {(cuuint32_t)p.CB, (cuuint32_t)L.NT, (cuuint32_t)(p.kh * L.rb)};
+            if (g_encode(&L.map_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box2,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cuda_fail("cuTensorMapEncodeTiled (w, two-frame stages)");
+        }
     }
     L.has_cache = cache_in != nullptr && P > 0;
     L.bias = b;
@@ -560,7 +568,8 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
     L.status = d->status;
     L.wait_ns = p.wait_ns;
     L.fault = p.fault;
-    const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * T * L.ncoblk;
+    // tiles: one per output frame, or per pair of output frames in the two-frame schedule
+    const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * (L.tstack ? (T + 1) / 2 : T) * L.ncoblk;
     if (L.pair) {
         const int npairs = (ntiles + 1) / 2;
         L.grid = 2 * (npairs < d->sms / 2 ? npairs : d->sms / 2);

@@ -42,6 +42,7 @@ struct TcLaunch {
     CUtensorMap map_x;      // x_chunk   [T][H][W][Cin]   box (CB, Sp, nrows, 1)
     CUtensorMap map_cache;  // cache_in  [P][H][W][Cin]   same box (unused if no cache)
     CUtensorMap map_w;      // w viewed as (Cin, Cout, taps) box (CB, NT, ks * rb)
+    CUtensorMap map_w2;     // two-frame SM-pair schedule: the same view, box (CB, Cout, ks)
     int T, H, W, Cin, Cout;
     int kt, ks;             // temporal extent (1..3) and spatial extent kh = kw (1 or 3)
     int up2;                // nearest-2x upsampling fused: H x W source frames, 2H x 2W outputs
@@ -52,6 +53,7 @@ struct TcLaunch {
     int issuers;                      // MMA-issuing warps (1 or 2)
     int rb;                           // kernel rows (of ks taps) per B stage: 1 or 3 (1 when ks == 1)
     int pair;                         // 1: SM-pair kernel (cta_group::2), weight rows split in two
+    int tstack;                       // 1: SM pairs with two output frames stacked into N per MMA
     int split_n;                      // with 2 issuers: split by N slice (else by 128-row group)
     int a_stage_bytes, b_stage_bytes;
     int tmem_cols;                    // allocated columns (power of two)
@@ -77,6 +79,7 @@ bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks
                   TcLaunch* L);
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 cudaError_t tc2_launch(int CB, const TcLaunch& L, cudaStream_t stream);
+cudaError_t tc2s_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 
 // Narrow-output kernel (Cout <= 5): the nine spatial taps stacked into N, rows streamed once.
 struct HeadLaunch {

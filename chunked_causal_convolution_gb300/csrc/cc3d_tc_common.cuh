@@ -58,13 +58,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return (uint32_t)__bfloat16_as_ushort(l) | ((uint32_t)__bfloat16_as_ushort(h) << 16);
 }
 
+// 16 bias values from shared memory as four 16-byte broadcast loads (co0 is a multiple of 16 and
+// the bias array is 16-byte aligned): a quarter of the shared-memory wavefronts of scalar loads,
+// which share the data path with the tensor core's operand reads.
+__device__ __forceinline__ void load_bias16(const float* s_bias, int co0, float* b)
+{
+    const float4* p = reinterpret_cast<const float4*>(s_bias + co0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 q = p[k];
+        b[4 * k] = q.x;
+        b[4 * k + 1] = q.y;
+        b[4 * k + 2] = q.z;
+        b[4 * k + 3] = q.w;
+    }
+}
+
 // 16 accumulator columns of one output position: + bias (+ residual) -> bf16 -> global.
 __device__ __forceinline__ void store16(const uint32_t* r, const float* s_bias, int co0, size_t px, int Cout,
                                         bool wide, const __nv_bfloat16* res, __nv_bfloat16* y)
 {
     float v[16];
+    load_bias16(s_bias, co0, v);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) v[k] = __fadd_rn(__uint_as_float(r[k]), s_bias[co0 + k]);
+    for (int k = 0; k < 16; ++k) v[k] = __fadd_rn(__uint_as_float(r[k]), v[k]);
     if (wide) {
         const size_t off = px * Cout + co0;
         if (res != nullptr) {
@@ -108,12 +125,13 @@ __device__ __forceinline__ void store16_res(const uint32_t* r, const float* s_bi
                                             const uint4 ra, const uint4 rb)
 {
     const uint32_t rr[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+    float bv[16];
+    load_bias16(s_bias, co0, bv);
     uint32_t o[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const float lo = __fadd_rn(__fadd_rn(__uint_as_float(r[2 * k]), s_bias[co0 + 2 * k]), bf16_lo(rr[k]));
-        const float hi =
-            __fadd_rn(__fadd_rn(__uint_as_float(r[2 * k + 1]), s_bias[co0 + 2 * k + 1]), bf16_hi(rr[k]));
+        const float lo = __fadd_rn(__fadd_rn(__uint_as_float(r[2 * k]), bv[2 * k]), bf16_lo(rr[k]));
+        const float hi = __fadd_rn(__fadd_rn(__uint_as_float(r[2 * k + 1]), bv[2 * k + 1]), bf16_hi(rr[k]));
         o[k] = pack_bf16x2(lo, hi);
     }
     reinterpret_cast<uint4*>(yp)[0] = make_uint4(o[0], o[1], o[2], o[3]);

@@ -496,3 +496,48 @@ def test_upsample_conv_matches_oracle_and_the_materialised_upsample(case):
     assert torch.equal(y, y_plain), (name, plain.kernel, int((y != y_plain).sum()))
     plain.close()
     plan.close()
+
+
+# ---------------------------------------------------------------- two-frame SM-pair schedule
+
+TSTACK = [
+    # name, Cin, Cout, T, H, W, chunks, bias, residual, kt
+    ("c96_residual_like", 96, 96, 7, 5, 256, [4, 3], True, True, 3),
+    ("kt2_memory_block", 64, 64, 6, 3, 128, [2, 4], True, False, 2),
+    ("cout128_full_tensor_memory", 32, 128, 5, 4, 128, [5], False, True, 3),
+    # 5 frames = 3 frame pairs (the last one half outside the chunk) on one row: 3 tiles, so the
+    # second pair of blocks also holds a phantom tile
+    ("odd_pairs_and_phantom_tile", 32, 32, 7, 1, 128, [5, 2], True, True, 3),
+]
+
+
+@pytest.mark.parametrize("case", TSTACK, ids=[c[0] for c in TSTACK])
+def test_two_frame_pair_schedule_is_bit_identical_to_the_one_frame_schedule(case, monkeypatch):
+    """Chunks of two or more frames on SM pairs stack two output frames into N; the one-frame pair
+    schedule (chosen for 1-frame chunks, or forced here through the tuning variable) accumulates
+    every output in the same order, so the two agree bit for bit, and both match the oracle."""
+    name, Cin, Cout, T, H, W, chunks, bias, residual, kt = case
+    raw = small_inputs(Cin, Cout, T, H, W, "bf16", 300 + len(name), bias, residual, k=(kt, 3, 3))
+    dev = {kk: to_device(v, "bf16") for kk, v in raw.items()}
+    plan = cc3d.CausalConv3dPlan(Cin, Cout, H, W, kt, 3, 3)
+    assert plan.kernel == "tc_bf16_pair"
+    y2, c2 = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), chunks)
+    assert plan.status() == 0
+    monkeypatch.setenv("CC3D_TC_TSTACK", "0")
+    y1, c1 = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), chunks)
+    assert plan.status() == 0
+    monkeypatch.delenv("CC3D_TC_TSTACK")
+    assert torch.equal(y2, y1), name
+    for a, b in zip(c2, c1):
+        assert torch.equal(a, b), name
+    ref = oracle.conv_whole(to_f64(raw["x"], "bf16"), to_f64(raw["w"], "bf16"),
+                            to_f64(raw["b"], "bf16") if bias else None,
+                            to_f64(raw["r"], "bf16") if residual else None)
+    err = np.abs(from_device(y2) - ref).max()
+    assert err <= tolerance("bf16", ref), (name, err)
+    # and across chunkings (1-frame chunks run the one-frame schedule)
+    for alt in ([T], [1] * T, [2] * (T // 2) + [1] * (T % 2)):
+        y3, _ = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), alt)
+        assert torch.equal(y3, y2), (name, alt)
+    assert plan.status() == 0
+    plan.close()

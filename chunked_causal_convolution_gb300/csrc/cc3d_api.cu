@@ -224,6 +224,7 @@ static cc3d_status stream_forward(const cc3d_plan_s& p, const DeviceInfo& d, int
     L.bias = b;
     L.res = res;
     L.y = y;
+    L.v32 = ((reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(res)) & 31) == 0 ? 1 : 0;
     L.status = d.status;
     L.wait_ns = p.wait_ns;
     L.fault = p.fault;
@@ -562,6 +563,7 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
     L.bias = b;
     L.res = res;
     L.y = y;
+    L.v32 = ((reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(res)) & 31) == 0 ? 1 : 0;
     L.x = x;
     L.cache_in = P > 0 ? cache_in : nullptr;
     L.cache_out = cache_out;

@@ -54,6 +54,7 @@ struct TcLaunch {
     int rb;                           // kernel rows (of ks taps) per B stage: 1 or 3 (1 when ks == 1)
     int pair;                         // 1: SM-pair kernel (cta_group::2), weight rows split in two
     int tstack;                       // 1: SM pairs with two output frames stacked into N per MMA
+    int v32;                          // y and the residual are 32-byte aligned: 32-byte epilogue accesses
     int split_n;                      // with 2 issuers: split by N slice (else by 128-row group)
     int a_stage_bytes, b_stage_bytes;
     int tmem_cols;                    // allocated columns (power of two)
@@ -126,6 +127,7 @@ struct StreamLaunch {
     const void* bias;           // bf16 [Cout] or null
     const void* res;            // bf16 [T][H][W][Cout] or null
     void* y;                    // bf16 [T][H][W][Cout]
+    int v32;                    // y and the residual 32-byte aligned: 32-byte epilogue accesses
     unsigned* status;
     unsigned long long wait_ns;
     int fault;

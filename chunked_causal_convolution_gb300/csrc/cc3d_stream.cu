@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
                 tc_fence_after();
                 const size_t px = pvalid ? (size_t)(g.t0 + tout) * (size_t)HW + (size_t)p : 0;
                 const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(tout * Cout);
-                epilogue_slice(tbase, Cout, 0, px, pvalid, true, s_bias, Cout, wide, res, y,
+                epilogue_slice(tbase, Cout, 0, px, pvalid, true, s_bias, Cout, wide, res, y, L.v32 != 0,
                                [&]() { release_acc(&acc_empty[tout], lane); });
             }
         }

@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
                                                (uint32_t)((m * 4 + cls) * NT);
                         const bool last_slice = (m == SUB - 1) && (cls == 3);
-                        epilogue_slice(tbase, NT, c.co0, px, valid, last_slice, s_bias, L.Cout, wide, res, y,
+                        epilogue_slice(tbase, NT, c.co0, px, valid, last_slice, s_bias, L.Cout, wide, res, y, L.v32 != 0,
                                        [&]() { release_acc(&acc_empty[as], lane); });
                     }
                     continue;
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                     const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
                                            (uint32_t)((m * nsplit + ns) * NT);
                     const bool last_slice = (m == SUB - 1) && (ns == nsplit - 1);
-                    epilogue_slice(tbase, NT, c.co0 + ns * NT, px, valid, last_slice, s_bias, L.Cout, wide, res, y,
+                    epilogue_slice(tbase, NT, c.co0 + ns * NT, px, valid, last_slice, s_bias, L.Cout, wide, res, y, L.v32 != 0,
                                    [&]() { release_acc(&acc_empty[as], lane); });
                 }
             }

@@ -333,7 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                            (uint32_t)((m * nsplit + ns) * NT);
                     const bool last_slice = (m == SUB - 1) && (ns == nsplit - 1);
                     // the release goes to the leader, whose MMA warps wait on it
-                    epilogue_slice(tbase, NT, c.co0 + ns * NT, px, valid, last_slice, s_bias, L.Cout, wide, res, y,
+                    epilogue_slice(tbase, NT, c.co0 + ns * NT, px, valid, last_slice, s_bias, L.Cout, wide, res, y, L.v32 != 0,
                                    [&]() {
                                        tc_fence_before();
                                        __syncwarp();

@@ -86,11 +86,30 @@ __device__ __forceinline__ void tmem_zero_quarter(uint32_t tbase, int NT)
     }
 }
 
-// bias (+ residual) and the bf16 stores of one quarter held in registers, 32 columns at a time
+// bias (+ residual) and the bf16 stores of one quarter held in registers, 32 columns at a time;
+// with `v32` every 16 channels move as one 32-byte load / store
 __device__ __forceinline__ void store_quarter(const uint32_t* r, int NT, size_t px, const float* s_bias, int Cout,
-                                              const __nv_bfloat16* res, __nv_bfloat16* y)
+                                              const __nv_bfloat16* res, __nv_bfloat16* y, bool v32)
 {
     __nv_bfloat16* yp = y + px * Cout;
+    if (v32) {
+#pragma unroll
+        for (int g = 0; g < 3; ++g) {
+            if (g * 32 + 16 > NT) break;
+            const bool two = g * 32 + 32 <= NT;
+            if (res != nullptr) {
+                uint32_t rr[16];
+                ld_nc_v8(res + px * Cout + g * 32, rr);
+                if (two) ld_nc_v8(res + px * Cout + g * 32 + 16, rr + 8);
+                store16_v8<true>(r + g * 32, s_bias, g * 32, yp + g * 32, rr);
+                if (two) store16_v8<true>(r + g * 32 + 16, s_bias, g * 32 + 16, yp + g * 32 + 16, rr + 8);
+            } else {
+                store16_v8<false>(r + g * 32, s_bias, g * 32, yp + g * 32, nullptr);
+                if (two) store16_v8<false>(r + g * 32 + 16, s_bias, g * 32 + 16, yp + g * 32 + 16, nullptr);
+            }
+        }
+        return;
+    }
     const uint4* rp = reinterpret_cast<const uint4*>(res + px * Cout);
 #pragma unroll
     for (int g = 0; g < 3; ++g) {
@@ -446,8 +465,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2s, 1)
                 release_to(half == 0 ? &accA_empty[0] : &accB_empty[0]);
                 release_to(half == 0 ? &accA_empty[1] : &accB_empty[1]);
                 size_t px;
-                if (position(0, &px)) store_quarter(r0, NT, px, s_bias, L.Cout, res, y);
-                if (position(1, &px)) store_quarter(r1, NT, px, s_bias, L.Cout, res, y);
+                if (position(0, &px)) store_quarter(r0, NT, px, s_bias, L.Cout, res, y, L.v32 != 0);
+                if (position(1, &px)) store_quarter(r1, NT, px, s_bias, L.Cout, res, y, L.v32 != 0);
             }
         }
     }

@@ -138,6 +138,43 @@ __device__ __forceinline__ void store16_res(const uint32_t* r, const float* s_bi
     reinterpret_cast<uint4*>(yp)[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// 32-byte global accesses (8 x 32 bits; the address must be 32-byte aligned): half the load /
+// store instructions of 16-byte ones for the same bytes
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* r)
+{
+    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void st_v8(void* p, const uint32_t* v)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+                 "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// 16 accumulator columns + bias (+ 16 bf16 residual values when RES) -> bf16 -> one 32-byte store
+template <bool RES>
+__device__ __forceinline__ void store16_v8(const uint32_t* r, const float* s_bias, int co0, __nv_bfloat16* yp,
+                                           const uint32_t* rr)
+{
+    float bv[16];
+    load_bias16(s_bias, co0, bv);
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        float lo = __fadd_rn(__uint_as_float(r[2 * k]), bv[2 * k]);
+        float hi = __fadd_rn(__uint_as_float(r[2 * k + 1]), bv[2 * k + 1]);
+        if (RES) {
+            lo = __fadd_rn(lo, bf16_lo(rr[k]));
+            hi = __fadd_rn(hi, bf16_hi(rr[k]));
+        }
+        o[k] = pack_bf16x2(lo, hi);
+    }
+    st_v8(yp, o);
+}
+
 // the epilogue warp is done reading this accumulator stage: let the MMA warps overwrite it
 __device__ __forceinline__ void release_acc(uint64_t* bar, int lane)
 {
@@ -150,12 +187,49 @@ __device__ __forceinline__ void release_acc(uint64_t* bar, int lane)
 // read from tensor memory 32 (or 16) at a time, + bias (+ residual), rounded to bf16 and stored.
 // `release()` runs once, right after the last columns are in registers, when `last` is set (the
 // accumulators may then be overwritten).  With a residual and NT <= 128 the whole residual row is
-// fetched in one batch first, so the thread waits for memory once per slice.
+// fetched in one batch first, so the thread waits for memory once per slice.  With `v32` (y and
+// the residual 32-byte aligned, Cout a multiple of 16) every 16 channels move as one 32-byte
+// access instead of two 16-byte ones.
 template <typename Release>
 __device__ __forceinline__ void epilogue_slice(uint32_t tbase, int NT, int co_base, size_t px, bool valid, bool last,
                                                const float* s_bias, int Cout, bool wide,
-                                               const __nv_bfloat16* res, __nv_bfloat16* y, Release release)
+                                               const __nv_bfloat16* res, __nv_bfloat16* y, bool v32,
+                                               Release release)
 {
+    if (res != nullptr && wide && NT <= 128 && v32) {
+        uint32_t rr[64];
+        const __nv_bfloat16* rp = res + px * Cout + co_base;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (valid && k * 16 < NT) {
+                ld_nc_v8(rp + k * 16, rr + 8 * k);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) rr[8 * k + u] = 0u;
+            }
+        }
+        __nv_bfloat16* yp = y + px * Cout + co_base;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            if (g * 32 + 32 <= NT) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + (uint32_t)(g * 32), r);
+                tmem_ld_wait();
+                if (last && g * 32 + 32 == NT) release();
+                if (valid) {
+                    store16_v8<true>(r, s_bias, co_base + g * 32, yp + g * 32, rr + 16 * g);
+                    store16_v8<true>(r + 16, s_bias, co_base + g * 32 + 16, yp + g * 32 + 16, rr + 16 * g + 8);
+                }
+            } else if (g * 32 + 16 == NT) {
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 32), r);
+                tmem_ld_wait();
+                if (last) release();
+                if (valid) store16_v8<true>(r, s_bias, co_base + g * 32, yp + g * 32, rr + 16 * g);
+            }
+        }
+        return;
+    }
     if (res != nullptr && wide && NT <= 128) {
         uint4 rv[16];
         const uint4* rp = reinterpret_cast<const uint4*>(res + px * Cout + co_base);
@@ -184,6 +258,7 @@ __device__ __forceinline__ void epilogue_slice(uint32_t tbase, int NT, int co_ba
         }
         return;
     }
+    const bool wide32 = v32 && wide && res == nullptr;
     int cc = 0;
     for (; cc + 32 <= NT; cc += 32) {
         uint32_t r[32];
@@ -191,8 +266,13 @@ __device__ __forceinline__ void epilogue_slice(uint32_t tbase, int NT, int co_ba
         tmem_ld_wait();
         if (last && cc + 32 == NT) release();
         if (valid) {
-            store16(r, s_bias, co_base + cc, px, Cout, wide, res, y);
-            store16(r + 16, s_bias, co_base + cc + 16, px, Cout, wide, res, y);
+            if (wide32) {
+                store16_v8<false>(r, s_bias, co_base + cc, y + px * Cout + co_base + cc, nullptr);
+                store16_v8<false>(r + 16, s_bias, co_base + cc + 16, y + px * Cout + co_base + cc + 16, nullptr);
+            } else {
+                store16(r, s_bias, co_base + cc, px, Cout, wide, res, y);
+                store16(r + 16, s_bias, co_base + cc + 16, px, Cout, wide, res, y);
+            }
         }
     }
     if (cc < NT) {  // NT % 32 == 16
@@ -200,7 +280,12 @@ __device__ __forceinline__ void epilogue_slice(uint32_t tbase, int NT, int co_ba
         tmem_ld_32x32b_x16(tbase + (uint32_t)cc, r);
         tmem_ld_wait();
         if (last) release();
-        if (valid) store16(r, s_bias, co_base + cc, px, Cout, wide, res, y);
+        if (valid) {
+            if (wide32)
+                store16_v8<false>(r, s_bias, co_base + cc, y + px * Cout + co_base + cc, nullptr);
+            else
+                store16(r, s_bias, co_base + cc, px, Cout, wide, res, y);
+        }
     }
 }
 

@@ -34,7 +34,8 @@
  *    4 bytes for every pointer; bfloat16 plans need 16 bytes for x_chunk, w,
  *    cache_in and cache_out (tensor-memory-accelerator copies), 16 bytes for
  *    y and residual when Cout is a multiple of 16 (2 bytes for the narrow
- *    head, Cout < 16), and 2 bytes for b.
+ *    head, Cout < 16), and 2 bytes for b.  (y and residual 32-byte aligned
+ *    let the SM-pair kernels use 32-byte accesses; results are the same.)
  *  - Layouts are dense row-major (channels innermost):
  *      x_chunk, residual, y : [T_chunk][H][W][C]
  *      cache_in, cache_out  : [kt-1][H][W][Cin]

@@ -503,7 +503,7 @@ def test_upsample_conv_matches_oracle_and_the_materialised_upsample(case):
 TSTACK = [
     # name, Cin, Cout, T, H, W, chunks, bias, residual, kt
     ("c96_residual_like", 96, 96, 7, 5, 256, [4, 3], True, True, 3),
-    ("kt2_memory_block", 64, 64, 6, 3, 128, [2, 4], True, False, 2),
+    ("c64_two_and_four_frame_chunks", 64, 64, 6, 3, 128, [2, 4], True, False, 3),
     ("cout128_full_tensor_memory", 32, 128, 5, 4, 128, [5], False, True, 3),
     # 5 frames = 3 frame pairs (the last one half outside the chunk) on one row: 3 tiles, so the
     # second pair of blocks also holds a phantom tile
@@ -540,4 +540,41 @@ def test_two_frame_pair_schedule_is_bit_identical_to_the_one_frame_schedule(case
         y3, _ = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), alt)
         assert torch.equal(y3, y2), (name, alt)
     assert plan.status() == 0
+    plan.close()
+
+
+ALIGN16 = [
+    # Cin, Cout, T, H, W, (kt, kh, kw), chunk, family
+    (96, 96, 4, 3, 128, (3, 3, 3), 4, "tc_bf16_pair"),      # two-frame schedule
+    (96, 96, 1, 3, 128, (3, 3, 3), 1, "tc_bf16_pair"),      # one-frame schedule
+    (64, 64, 3, 4, 40, (3, 3, 3), 3, "tc_bf16"),            # one SM
+    (32, 384, 2, 3, 20, (3, 3, 3), 2, "tc_bf16"),           # channel blocks
+    (96, 96, 3, 2, 70, (3, 1, 1), 3, "tc_bf16_stream"),
+]
+
+
+@pytest.mark.parametrize("case", ALIGN16, ids=["%s_T%d_c%d" % (c[-1], c[2], c[1]) for c in ALIGN16])
+def test_outputs_and_residual_only_16_byte_aligned(case):
+    """y and the residual 16 but not 32 bytes aligned: the epilogues take their 16-byte accesses
+    and the result is bit-identical to the one with 32-byte aligned buffers."""
+    Cin, Cout, T, H, W, k, chunk, family = case
+    raw = small_inputs(Cin, Cout, T, H, W, "bf16", 77, True, True, k=k)
+    dev = {kk: to_device(v, "bf16") for kk, v in raw.items()}
+    plan = cc3d.CausalConv3dPlan(Cin, Cout, H, W, *k)
+    assert plan.kernel == family
+    y_ref, _ = run_chunks(plan, dev["x"], dev["w"], dev["b"], dev["r"], [chunk] * (T // chunk))
+    n = T * H * W * Cout
+    rbuf = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+    ybuf = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+    r16 = rbuf[8:].view(T, H, W, Cout)
+    y16 = ybuf[8:].view(T, H, W, Cout)
+    assert r16.data_ptr() % 32 == 16 and y16.data_ptr() % 32 == 16
+    r16.copy_(dev["r"])
+    cache = [None, plan.new_cache(), plan.new_cache()]
+    for j in range(T // chunk):
+        s0 = j * chunk
+        plan.forward_chunk(dev["x"][s0:s0 + chunk], dev["w"], dev["b"], r16[s0:s0 + chunk],
+                           cache[j % 2 + 1] if j else None, cache[(j + 1) % 2 + 1], y16[s0:s0 + chunk])
+    assert plan.status() == 0
+    assert torch.equal(y16, y_ref)
     plan.close()

@@ -314,38 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
     } else if (warp == 2 || warp == 3) {
         // ------------------------------------------------------------ temporal cache update
-        // cache_out[j] = frame (T + j) of concat(cache_in, x); j < 2.  Warps 2-3, or warp 3 alone
-        // when warp 2 issues MMAs.
-        const int cthreads = nissue == 2 ? 32 : 64;
-        const int ctid = threadIdx.x - (nissue == 2 ? 96 : 64);
-        const size_t frame_chunks = (size_t)L.H * L.W * L.Cin * 2 / 16;
-        const size_t total = (size_t)P * frame_chunks;
-        const size_t gthreads = (size_t)gridDim.x * cthreads;
-        const uint4* xin = reinterpret_cast<const uint4*>(L.x);
-        const uint4* cin = reinterpret_cast<const uint4*>(L.cache_in);
-        uint4* cout_ = reinterpret_cast<uint4*>(L.cache_out);
-        // 16 independent 16-byte loads in flight per thread before their stores
-        constexpr int U = 16;
-        for (size_t i0 = ((size_t)blockIdx.x * cthreads + ctid) * U; i0 < total; i0 += gthreads * U) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const size_t i = i0 + u;
-                v[u] = make_uint4(0, 0, 0, 0);
-                if (i < total) {
-                    const int j = (int)(i / frame_chunks);
-                    const size_t o = i - (size_t)j * frame_chunks;
-                    const int src = L.T + j;  // index in the extended stack
-                    if (src >= P)
-                        v[u] = __ldg(xin + (size_t)(src - P) * frame_chunks + o);
-                    else if (cin != nullptr)
-                        v[u] = __ldg(cin + (size_t)src * frame_chunks + o);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (i0 + u < total) __stcs(cout_ + i0 + u, v[u]);
-        }
+        // Warps 2-3, or warp 3 alone when warp 2 issues MMAs.
+        const int nw = nissue == 2 ? 1 : 2;
+        copy_history(L, P, warp - (nissue == 2 ? 3 : 2), nw, lane);
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp - 4;  // tensor-memory lanes 32q .. 32q+31

@@ -365,33 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2s, 1)
             atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
     } else if (warp == 3) {
         // ------------------------------------------------------------ temporal cache update
-        const size_t frame_chunks = (size_t)L.H * L.W * L.Cin * 2 / 16;
-        const size_t total = (size_t)P * frame_chunks;
-        const size_t gthreads = (size_t)gridDim.x * 32;
-        const uint4* xin = reinterpret_cast<const uint4*>(L.x);
-        const uint4* cin = reinterpret_cast<const uint4*>(L.cache_in);
-        uint4* cout_ = reinterpret_cast<uint4*>(L.cache_out);
-        constexpr int U = 16;
-        for (size_t i0 = ((size_t)blockIdx.x * 32 + lane) * U; i0 < total; i0 += gthreads * U) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const size_t i = i0 + u;
-                v[u] = make_uint4(0, 0, 0, 0);
-                if (i < total) {
-                    const int jf = (int)(i / frame_chunks);
-                    const size_t o = i - (size_t)jf * frame_chunks;
-                    const int src = L.T + jf;
-                    if (src >= P)
-                        v[u] = __ldg(xin + (size_t)(src - P) * frame_chunks + o);
-                    else if (cin != nullptr)
-                        v[u] = __ldg(cin + (size_t)src * frame_chunks + o);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (i0 + u < total) __stcs(cout_ + i0 + u, v[u]);
-        }
+        copy_history(L, P, 0, 1, lane);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue (both blocks)
         const int q = warp - 4;  // lane quadrant of tensor memory this warp may access

@@ -175,6 +175,45 @@ __device__ __forceinline__ void store16_v8(const uint32_t* r, const float* s_bia
     st_v8(yp, o);
 }
 
+// The temporal cache update done by otherwise idle warps: cache_out[j] = frame T + j of the
+// stack (the P cache_in frames, then the T frames of x; zeros for a missing cache_in), j < P.
+// `nwarps` warps of every block take part (this one is number `cw`).  In each 16-byte step the
+// 32 lanes of a warp cover 512 contiguous bytes, and each thread has 16 loads in flight before
+// its stores.
+__device__ __forceinline__ void copy_history(const TcLaunch& L, int P, int cw, int nwarps, int lane)
+{
+    const size_t frame_chunks = (size_t)L.H * L.W * L.Cin * 2 / 16;
+    const size_t total = (size_t)P * frame_chunks;
+    const uint4* xin = reinterpret_cast<const uint4*>(L.x);
+    const uint4* cin = reinterpret_cast<const uint4*>(L.cache_in);
+    uint4* cout_ = reinterpret_cast<uint4*>(L.cache_out);
+    constexpr int U = 16;
+    const size_t span = (size_t)32 * U;  // 16-byte elements of one warp step
+    const size_t stride = (size_t)gridDim.x * nwarps * span;
+    for (size_t base = ((size_t)blockIdx.x * nwarps + cw) * span; base < total; base += stride) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const size_t i = base + (size_t)u * 32 + lane;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (i < total) {
+                const int j = (int)(i / frame_chunks);
+                const size_t o = i - (size_t)j * frame_chunks;
+                const int src = L.T + j;  // index in the stack of cache_in and x frames
+                if (src >= P)
+                    v[u] = __ldg(xin + (size_t)(src - P) * frame_chunks + o);
+                else if (cin != nullptr)
+                    v[u] = __ldg(cin + (size_t)src * frame_chunks + o);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const size_t i = base + (size_t)u * 32 + lane;
+            if (i < total) __stcs(cout_ + i, v[u]);
+        }
+    }
+}
+
 // the epilogue warp is done reading this accumulator stage: let the MMA warps overwrite it
 __device__ __forceinline__ void release_acc(uint64_t* bar, int lane)
 {

@@ -117,7 +117,60 @@ struct cc3d_plan_s {
     int CB;
     unsigned long long wait_ns;
     int fault;
+    // The one-frame SM-pair kernel's new history is copied by a copy engine on a side stream,
+    // forked from the caller's stream before the launch and joined to it after (created on first
+    // use, on the device current then; on another device the kernel copies the history itself).
+    // Measured on GB300: 2x3x3 at 96 channels (one history frame) 1400 against 1315 TFLOP/s with
+    // the kernel's own copy warp; the other kernels are faster with their copy warp (a copy
+    // engine moves about 0.3 TB/s, and splitting the copy over more streams did not add to it).
+    static constexpr int kSide = 1;
+    cudaStream_t side[kSide] = {};
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join[kSide] = {};
+    int side_device = -1;
+    ~cc3d_plan_s()
+    {
+        for (int i = 0; i < kSide; ++i) {
+            if (side[i] != nullptr) cudaStreamDestroy(side[i]);
+            if (join[i] != nullptr) cudaEventDestroy(join[i]);
+        }
+        if (fork != nullptr) cudaEventDestroy(fork);
+    }
 };
+
+namespace {
+
+// The side streams and their events for this plan on the current device; false if they cannot be
+// had (then the kernel copies the history).
+bool side_stream_ready(cc3d_plan_s* p)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (p->fork != nullptr) return p->side_device == dev;
+    bool ok = cudaEventCreateWithFlags(&p->fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < cc3d_plan_s::kSide; ++i)
+        ok = cudaStreamCreateWithFlags(&p->side[i], cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p->join[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        for (int i = 0; i < cc3d_plan_s::kSide; ++i) {
+            if (p->side[i] != nullptr) cudaStreamDestroy(p->side[i]);
+            if (p->join[i] != nullptr) cudaEventDestroy(p->join[i]);
+            p->side[i] = nullptr;
+            p->join[i] = nullptr;
+        }
+        if (p->fork != nullptr) cudaEventDestroy(p->fork);
+        p->fork = nullptr;
+        return false;
+    }
+    p->side_device = dev;
+    return true;
+}
+
+}  // namespace
 
 // Narrow-output launch: tensor maps with one-row boxes for the staged input rows (loads) and the
 // new history (stores), and a (32 channels, Cout, 9 taps) box for the weights of one (dt,
@@ -578,8 +631,41 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
     } else {
         L.grid = ntiles < d->sms ? ntiles : d->sms;
     }
-    const cudaError_t e = tc_launch(p.CB, L, stream);
-    return e == cudaSuccess ? CC3D_OK : cuda_fail("tensor-core kernel launch", e);
+    // ---- the new history: cache_out slot j = frame T + j of the stack (cache_in frames, then x
+    // frames; zeros for a missing cache_in), moved by the copy engines while the kernel runs
+    const bool side_copy = P > 0 && L.pair && !L.tstack && side_stream_ready(plan);
+    L.copy_hist = (P > 0 && !side_copy) ? 1 : 0;
+    if (side_copy) {
+        // the history as one byte range of cache_out: the first jx slots from cache_in (or zeros),
+        // the rest from x; each side stream moves an equal share of it
+        const int jx = P > T ? P - T : 0;
+        const size_t n_in = (size_t)jx * frame_in, n_all = (size_t)P * frame_in;
+        const char* src_in = static_cast<const char*>(cache_in) + (size_t)T * frame_in;
+        const char* src_x = static_cast<const char*>(x) + (size_t)(T + jx - P) * frame_in - n_in;
+        char* dst = static_cast<char*>(cache_out);
+        const size_t share = ((n_all + cc3d_plan_s::kSide - 1) / cc3d_plan_s::kSide + 255) & ~size_t(255);
+        cudaError_t e = cudaEventRecord(plan->fork, stream);
+        for (int i = 0; e == cudaSuccess && i < cc3d_plan_s::kSide; ++i) {
+            cudaStream_t ss = plan->side[i];
+            e = cudaStreamWaitEvent(ss, plan->fork, 0);
+            const size_t a0 = (size_t)i * share < n_all ? (size_t)i * share : n_all;
+            const size_t a1 = a0 + share < n_all ? a0 + share : n_all;
+            // [a0, a1) split at n_in into its cache_in part and its x part
+            const size_t m = a1 < n_in ? a1 : (a0 > n_in ? a0 : n_in);
+            if (e == cudaSuccess && m > a0)
+                e = cache_in != nullptr ? cudaMemcpyAsync(dst + a0, src_in + a0, m - a0, cudaMemcpyDeviceToDevice, ss)
+                                        : cudaMemsetAsync(dst + a0, 0, m - a0, ss);
+            if (e == cudaSuccess && a1 > m) e = cudaMemcpyAsync(dst + m, src_x + m, a1 - m, cudaMemcpyDeviceToDevice, ss);
+            if (e == cudaSuccess) e = cudaEventRecord(plan->join[i], ss);
+        }
+        if (e != cudaSuccess) return cuda_fail("history copy on the side streams", e);
+    }
+    cudaError_t e = tc_launch(p.CB, L, stream);
+    if (e != cudaSuccess) return cuda_fail("tensor-core kernel launch", e);
+    for (int i = 0; side_copy && i < cc3d_plan_s::kSide; ++i)
+        if ((e = cudaStreamWaitEvent(stream, plan->join[i], 0)) != cudaSuccess)
+            return cuda_fail("join of the history copy", e);
+    return CC3D_OK;
 }
 
 extern "C" {

@@ -63,7 +63,9 @@ struct TcLaunch {
     const void* bias;                 // bf16 [Cout] or null
     const void* res;                  // bf16 [T][H][W][Cout] or null
     void* y;                          // bf16 [T][H][W][Cout]
-    // temporal cache update (done by otherwise idle warps)
+    // temporal cache update (done by otherwise idle warps when copy_hist is set; otherwise the
+    // host has the copy engines move it beside the kernel)
+    int copy_hist;
     const void* x;
     const void* cache_in;
     void* cache_out;

@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         // ------------------------------------------------------------ temporal cache update
         // Warps 2-3, or warp 3 alone when warp 2 issues MMAs.
         const int nw = nissue == 2 ? 1 : 2;
-        copy_history(L, P, warp - (nissue == 2 ? 3 : 2), nw, lane);
+        if (L.copy_hist) copy_history(L, P, warp - (nissue == 2 ? 3 : 2), nw, lane);
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp - 4;  // tensor-memory lanes 32q .. 32q+31

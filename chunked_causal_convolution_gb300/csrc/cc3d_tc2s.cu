@@ -365,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2s, 1)
             atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
     } else if (warp == 3) {
         // ------------------------------------------------------------ temporal cache update
-        copy_history(L, P, 0, 1, lane);
+        if (L.copy_hist) copy_history(L, P, 0, 1, lane);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue (both blocks)
         const int q = warp - 4;  // lane quadrant of tensor memory this warp may access

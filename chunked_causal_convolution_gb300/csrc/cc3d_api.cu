@@ -633,13 +633,18 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
     }
     // ---- the new history: cache_out slot j = frame T + j of the stack (cache_in frames, then x
     // frames; zeros for a missing cache_in), moved by the copy engines while the kernel runs
-    const bool side_copy = P > 0 && L.pair && !L.tstack && side_stream_ready(plan);
-    L.copy_hist = (P > 0 && !side_copy) ? 1 : 0;
+    // Slots [0, n_ce) go to the copy engine: all of them for the one-frame pair kernel, the first
+    // of the two-frame kernel's (one 2-frame history would outlast its launch on one engine), none
+    // for the one-SM kernel.
+    const int n_ce = P == 0 ? 0 : (L.pair && !L.tstack ? P : (L.tstack ? 1 : 0));
+    const bool side_copy = n_ce > 0 && side_stream_ready(plan);
+    L.hist_from = side_copy ? n_ce : 0;
+    L.copy_hist = L.hist_from < P ? 1 : 0;
     if (side_copy) {
-        // the history as one byte range of cache_out: the first jx slots from cache_in (or zeros),
-        // the rest from x; each side stream moves an equal share of it
+        // slots [0, n_ce) of cache_out as one byte range: the first jx slots from cache_in (or
+        // zeros), the rest from x; each side stream moves an equal share of it
         const int jx = P > T ? P - T : 0;
-        const size_t n_in = (size_t)jx * frame_in, n_all = (size_t)P * frame_in;
+        const size_t n_in = (size_t)(jx < n_ce ? jx : n_ce) * frame_in, n_all = (size_t)n_ce * frame_in;
         const char* src_in = static_cast<const char*>(cache_in) + (size_t)T * frame_in;
         const char* src_x = static_cast<const char*>(x) + (size_t)(T + jx - P) * frame_in - n_in;
         char* dst = static_cast<char*>(cache_out);

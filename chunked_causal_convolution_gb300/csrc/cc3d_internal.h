@@ -63,9 +63,10 @@ struct TcLaunch {
     const void* bias;                 // bf16 [Cout] or null
     const void* res;                  // bf16 [T][H][W][Cout] or null
     void* y;                          // bf16 [T][H][W][Cout]
-    // temporal cache update (done by otherwise idle warps when copy_hist is set; otherwise the
-    // host has the copy engines move it beside the kernel)
+    // temporal cache update: history slots hist_from .. P-1 are copied by otherwise idle warps
+    // when copy_hist is set, the slots before hist_from by a copy engine beside the kernel
     int copy_hist;
+    int hist_from;
     const void* x;
     const void* cache_in;
     void* cache_out;

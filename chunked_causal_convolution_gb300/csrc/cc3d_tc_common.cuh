@@ -176,7 +176,8 @@ __device__ __forceinline__ void store16_v8(const uint32_t* r, const float* s_bia
 }
 
 // The temporal cache update done by otherwise idle warps: cache_out[j] = frame T + j of the
-// stack (the P cache_in frames, then the T frames of x; zeros for a missing cache_in), j < P.
+// stack (the P cache_in frames, then the T frames of x; zeros for a missing cache_in), for
+// hist_from <= j < P (the host has a copy engine move the slots before hist_from).
 // `nwarps` warps of every block take part (this one is number `cw`).  In each 16-byte step the
 // 32 lanes of a warp cover 512 contiguous bytes, and each thread has 16 loads in flight before
 // its stores.
@@ -184,13 +185,14 @@ __device__ __forceinline__ void copy_history(const TcLaunch& L, int P, int cw, i
 {
     const size_t frame_chunks = (size_t)L.H * L.W * L.Cin * 2 / 16;
     const size_t total = (size_t)P * frame_chunks;
+    const size_t first = (size_t)L.hist_from * frame_chunks;  // slots before hist_from: copy engine
     const uint4* xin = reinterpret_cast<const uint4*>(L.x);
     const uint4* cin = reinterpret_cast<const uint4*>(L.cache_in);
     uint4* cout_ = reinterpret_cast<uint4*>(L.cache_out);
     constexpr int U = 16;
     const size_t span = (size_t)32 * U;  // 16-byte elements of one warp step
     const size_t stride = (size_t)gridDim.x * nwarps * span;
-    for (size_t base = ((size_t)blockIdx.x * nwarps + cw) * span; base < total; base += stride) {
+    for (size_t base = first + ((size_t)blockIdx.x * nwarps + cw) * span; base < total; base += stride) {
         uint4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {

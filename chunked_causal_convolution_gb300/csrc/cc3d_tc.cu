@@ -502,11 +502,11 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
         acc = env_int("CC3D_TC_ACC", 2);
     }
     // two output frames per pair tile, stacked into N where an input frame is a tap of both
-    // (chunks of two or more frames of a 3 x 3 x 3 kernel, up to 96 output channels; with kt = 2
-    // only one of three input frames is shared and it measured 1 % slower): two row groups per
+    // (chunks of two or more frames of a kt x 3 x 3 kernel with kt >= 2, up to 96 output channels;
+    // with kt = 2 one of three input frames is shared, measured 1 % faster): two row groups per
     // block, one accumulator buffer of 2 frames x 2 row groups x NT columns
     L->tstack = 0;
-    if (L->pair && kt == 3 && ks == 3 && T >= 2 && L->NT <= 96 && sub_cap >= 2 && env_int("CC3D_TC_TSTACK", 1)) {
+    if (L->pair && kt >= 2 && ks == 3 && T >= 2 && L->NT <= 96 && sub_cap >= 2 && env_int("CC3D_TC_TSTACK", 1)) {
         L->tstack = 1;
         sub = 2;
         acc = 1;

@@ -504,6 +504,7 @@ TSTACK = [
     # name, Cin, Cout, T, H, W, chunks, bias, residual, kt
     ("c96_residual_like", 96, 96, 7, 5, 256, [4, 3], True, True, 3),
     ("c64_two_and_four_frame_chunks", 64, 64, 6, 3, 128, [2, 4], True, False, 3),
+    ("kt2_memory_block", 96, 96, 7, 3, 128, [4, 3], True, True, 2),
     ("cout128_full_tensor_memory", 32, 128, 5, 4, 128, [5], False, True, 3),
     # 5 frames = 3 frame pairs (the last one half outside the chunk) on one row: 3 tiles, so the
     # second pair of blocks also holds a phantom tile

@@ -123,6 +123,13 @@ cc3d_status cc3d_plan_create_upsample2x(int Cin, int Cout, int H, int W, int kt,
  * split into chunks (bit-identical across chunkings).
  * Returns CC3D_OK once the work is enqueued; asynchronous failures surface in
  * cc3d_get_status.
+ * Stream use: all work is ordered after what the caller enqueued earlier on
+ * `stream`, and everything the caller enqueues on it afterwards sees y and
+ * cache_out complete.  For the SM-pair tensor-core kernels part of the
+ * cache_out copy runs on a copy engine, on a side stream the plan creates on
+ * its first such call (with two events; freed by cc3d_destroy): an event
+ * forks it from `stream` before the kernel and `stream` waits for it after.
+ * The call therefore stays capturable into a CUDA graph on `stream`.
  */
 cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T_chunk, const void* x_chunk, const void* w, const void* b,
                                const void* residual_or_null, const void* cache_in, void* cache_out, void* y,

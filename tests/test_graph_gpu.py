@@ -97,3 +97,57 @@ def test_graph_replay_of_a_two_layer_chunk_is_bit_identical():
     assert np.abs(from_device(y_eager) - y_ref).max() <= tolerance("bf16", y_ref)
     conv.close()
     head.close()
+
+
+@pytest.mark.parametrize("Tc", [2, 1])
+def test_graph_replay_of_sm_pair_chunks_with_the_side_stream_copy(Tc):
+    """SM-pair layers move part of the history on a copy engine through a side stream forked from
+    and joined to the caller's stream (all of it for 1-frame chunks, one frame of it for 2-frame
+    chunks).  Captured into CUDA graphs and replayed, outputs and histories are bit-identical to
+    the eager chunk loop."""
+    T, H, W, C = 6, 3, 128, 64
+    a = small_inputs(C, C, T, H, W, "bf16", 81, bias=True, residual=True)
+    x, r = to_device(a["x"], "bf16"), to_device(a["r"], "bf16")
+    w, b = to_device(a["w"], "bf16"), to_device(a["b"], "bf16")
+    plan = cc3d.CausalConv3dPlan(C, C, H, W)
+    assert plan.kernel == "tc_bf16_pair"
+    c = [plan.new_cache(), plan.new_cache()]
+    ys = []
+    for k in range(T // Tc):
+        ys.append(plan.forward_chunk(x[k * Tc:(k + 1) * Tc], w, b, r[k * Tc:(k + 1) * Tc],
+                                     c[k % 2] if k else None, c[(k + 1) % 2]))
+    y_eager = torch.cat(ys)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+
+    xs = torch.empty((Tc, H, W, C), dtype=torch.bfloat16, device="cuda")
+    rs = torch.empty_like(xs)
+    ybuf = torch.empty_like(xs)
+    g = [plan.new_cache(), plan.new_cache()]
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for parity in range(2):
+            plan.forward_chunk(xs, w, b, rs, g[parity], g[1 - parity], ybuf, stream=stream)
+        stream.synchronize()
+        for parity in range(2):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                plan.forward_chunk(xs, w, b, rs, g[parity], g[1 - parity], ybuf, stream=stream)
+            graphs.append(gr)
+    plan.reset(g[0])
+    outs = []
+    for k in range(T // Tc):
+        xs.copy_(x[k * Tc:(k + 1) * Tc])
+        rs.copy_(r[k * Tc:(k + 1) * Tc])
+        graphs[k % 2].replay()
+        outs.append(ybuf.clone())
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    assert torch.equal(torch.cat(outs), y_eager)
+    last = (T // Tc) % 2
+    assert torch.equal(g[last], c[last])
+    ref = oracle.conv_whole(to_f64(a["x"], "bf16"), to_f64(a["w"], "bf16"), to_f64(a["b"], "bf16"),
+                            to_f64(a["r"], "bf16"))
+    assert np.abs(from_device(y_eager) - ref).max() <= tolerance("bf16", ref)
+    plan.close()

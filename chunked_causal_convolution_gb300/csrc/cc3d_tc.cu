@@ -86,7 +86,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         // stage releases and accumulator completions come from every MMA warp
         for (int s = 0; s < L.na; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], nissue); }
         for (int s = 0; s < L.nb; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], nissue); }
-        for (int a = 0; a < L.acc_stages; ++a) { mbar_init(&acc_full[a], nissue); mbar_init(&acc_empty[a], 4); }
+        for (int a = 0; a < L.acc_stages; ++a) mbar_init(&acc_full[a], nissue);
+        // released by the 4 epilogue warps; an upsampling layer (one accumulator stage) releases
+        // the two MMA warps' class pairs separately, on acc_empty[0] and acc_empty[1]
+        for (int a = 0; a < (L.up2 ? 2 : L.acc_stages); ++a) mbar_init(&acc_empty[a], 4);
         mbar_init(&mma_drain[0], 1);
         mbar_init(&mma_drain[1], 1);
         fence_mbar_init();
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             const TileCoord c = tile_coord(L, tile);
             const int as = it % L.acc_stages;
             const int aph = (it / L.acc_stages) & 1;
-            if (!warp_bounded_wait(&acc_empty[as], aph ^ 1, budget, &abort_flag)) {
+            if (!warp_bounded_wait(&acc_empty[L.up2 ? k : as], aph ^ 1, budget, &abort_flag)) {
                 if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
                 break;
             }
@@ -351,27 +354,53 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             ready = __shfl_sync(0xffffffffu, ready, 0);
             if (!ready) break;
             tc_fence_after();
+            if (L.up2) {
+                // class (a, b) of source pixel (h, w) is output pixel (2h + a, 2w + b) of the
+                // 2H x 2W frame.  Class pair kp belongs to MMA warp kp and is released on
+                // acc_empty[kp] once its columns of the last row group are in registers: with NT
+                // <= 96 each class is read whole before its stores, so an MMA warp waits for its
+                // own classes only, and for the stores of one of them.
+                for (int kp = 0; kp < 2; ++kp) {
+                    for (int m = 0; m < SUB; ++m) {
+                        const int f = c.f0 + m * L.g.sub_stride + q * 32 + lane;
+                        const int h = f / Sp;
+                        const int jcol = f - h * Sp;
+                        const int w = c.w0 + jcol - 1;
+                        const bool valid = h < L.H && jcol >= 1 && jcol <= L.g.S && w < L.W;
+                        const bool last_m = m == SUB - 1;
+                        // output position of class 2 kp + u of this lane's source pixel
+                        auto out_px = [&](int u) {
+                            const int cls = 2 * kp + u;
+                            const size_t oh = valid ? 2 * (size_t)h + (cls >> 1) : 0;
+                            const size_t ow = valid ? 2 * (size_t)w + (cls & 1) : 0;
+                            return ((size_t)c.t * 2 * L.H + oh) * 2 * L.W + ow;
+                        };
+                        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
+                                            (uint32_t)((m * 4 + 2 * kp) * NT);
+                        if (NT <= 96 && wide) {
+                            for (int u = 0; u < 2; ++u) {
+                                uint32_t r[96];
+                                tmem_read_quarter(tb + (uint32_t)(u * NT), NT, r);
+                                tmem_ld_wait();
+                                if (last_m && u == 1) release_acc(&acc_empty[kp], lane);
+                                if (valid) store_quarter(r, NT, c.co0, out_px(u), s_bias, L.Cout, res, y, L.v32 != 0);
+                            }
+                        } else {
+                            for (int u = 0; u < 2; ++u)
+                                epilogue_slice(tb + (uint32_t)(u * NT), NT, c.co0, out_px(u), valid, last_m && u == 1, s_bias,
+                                               L.Cout, wide, res, y, L.v32 != 0,
+                                               [&]() { release_acc(&acc_empty[kp], lane); });
+                        }
+                    }
+                }
+                continue;
+            }
             for (int m = 0; m < SUB; ++m) {
                 const int f = c.f0 + m * L.g.sub_stride + q * 32 + lane;
                 const int h = f / Sp;
                 const int jcol = f - h * Sp;
                 const int w = c.w0 + jcol - 1;
                 const bool valid = h < L.H && jcol >= 1 && jcol <= L.g.S && w < L.W;
-                if (L.up2) {
-                    // class (a, b) of source pixel (h, w) is output pixel (2h + a, 2w + b) of the
-                    // 2H x 2W frame
-                    for (int cls = 0; cls < 4; ++cls) {
-                        const size_t oh = valid ? 2 * (size_t)h + (cls >> 1) : 0;
-                        const size_t ow = valid ? 2 * (size_t)w + (cls & 1) : 0;
-                        const size_t px = ((size_t)c.t * 2 * L.H + oh) * 2 * L.W + ow;
-                        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
-                                               (uint32_t)((m * 4 + cls) * NT);
-                        const bool last_slice = (m == SUB - 1) && (cls == 3);
-                        epilogue_slice(tbase, NT, c.co0, px, valid, last_slice, s_bias, L.Cout, wide, res, y, L.v32 != 0,
-                                       [&]() { release_acc(&acc_empty[as], lane); });
-                    }
-                    continue;
-                }
                 const size_t px = ((size_t)c.t * L.H + (valid ? h : 0)) * L.W + (valid ? w : 0);
                 for (int ns = 0; ns < nsplit; ++ns) {
                     const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +

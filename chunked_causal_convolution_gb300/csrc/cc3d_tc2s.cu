@@ -60,74 +60,6 @@ __device__ __forceinline__ TileCoord frame_pair_tile(const TcLaunch& L, int tile
     return c;
 }
 
-// The accumulator columns of one frame in both row groups (NT <= 96 fp32 columns each) for this
-// thread's lane: all are read out first (and, with `zero`, overwritten with zeros), then
-// `release(m)` hands row group m back to its MMA warp, and only then come the residual loads and
-// the stores: the MMA warps wait for tensor-memory reads only, never for memory latency.
-__device__ __forceinline__ void tmem_read_quarter(uint32_t tbase, int NT, uint32_t* r)
-{
-#pragma unroll
-    for (int g = 0; g < 3; ++g) {
-        if (g * 32 + 32 <= NT)
-            tmem_ld_32x32b_x32(tbase + (uint32_t)(g * 32), r + g * 32);
-        else if (g * 32 + 16 == NT)
-            tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 32), r + g * 32);
-    }
-}
-
-__device__ __forceinline__ void tmem_zero_quarter(uint32_t tbase, int NT)
-{
-#pragma unroll
-    for (int g = 0; g < 3; ++g) {
-        if (g * 32 + 32 <= NT)
-            tmem_st_32x32b_x32_zero(tbase + (uint32_t)(g * 32));
-        else if (g * 32 + 16 == NT)
-            tmem_st_32x32b_x16_zero(tbase + (uint32_t)(g * 32));
-    }
-}
-
-// bias (+ residual) and the bf16 stores of one quarter held in registers, 32 columns at a time;
-// with `v32` every 16 channels move as one 32-byte load / store
-__device__ __forceinline__ void store_quarter(const uint32_t* r, int NT, size_t px, const float* s_bias, int Cout,
-                                              const __nv_bfloat16* res, __nv_bfloat16* y, bool v32)
-{
-    __nv_bfloat16* yp = y + px * Cout;
-    if (v32) {
-#pragma unroll
-        for (int g = 0; g < 3; ++g) {
-            if (g * 32 + 16 > NT) break;
-            const bool two = g * 32 + 32 <= NT;
-            if (res != nullptr) {
-                uint32_t rr[16];
-                ld_nc_v8(res + px * Cout + g * 32, rr);
-                if (two) ld_nc_v8(res + px * Cout + g * 32 + 16, rr + 8);
-                store16_v8<true>(r + g * 32, s_bias, g * 32, yp + g * 32, rr);
-                if (two) store16_v8<true>(r + g * 32 + 16, s_bias, g * 32 + 16, yp + g * 32 + 16, rr + 8);
-            } else {
-                store16_v8<false>(r + g * 32, s_bias, g * 32, yp + g * 32, nullptr);
-                if (two) store16_v8<false>(r + g * 32 + 16, s_bias, g * 32 + 16, yp + g * 32 + 16, nullptr);
-            }
-        }
-        return;
-    }
-    const uint4* rp = reinterpret_cast<const uint4*>(res + px * Cout);
-#pragma unroll
-    for (int g = 0; g < 3; ++g) {
-        if (g * 32 + 16 > NT) break;
-        const bool two = g * 32 + 32 <= NT;
-        if (res != nullptr) {
-            uint4 rv[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) rv[k] = (k < 2 || two) ? __ldg(rp + 4 * g + k) : make_uint4(0, 0, 0, 0);
-            store16_res(r + g * 32, s_bias, g * 32, yp + g * 32, rv[0], rv[1]);
-            if (two) store16_res(r + g * 32 + 16, s_bias, g * 32 + 16, yp + g * 32 + 16, rv[2], rv[3]);
-        } else {
-            store16(r + g * 32, s_bias, g * 32, px, Cout, true, nullptr, y);
-            if (two) store16(r + g * 32 + 16, s_bias, g * 32 + 16, px, Cout, true, nullptr, y);
-        }
-    }
-}
-
 // the residual rows of this thread's output position, warmed in L2 while the accumulators fill
 __device__ __forceinline__ void prefetch_residual(const __nv_bfloat16* res, size_t px, int Cout, bool valid)
 {
@@ -439,8 +371,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2s, 1)
                 release_to(half == 0 ? &accA_empty[0] : &accB_empty[0]);
                 release_to(half == 0 ? &accA_empty[1] : &accB_empty[1]);
                 size_t px;
-                if (position(0, &px)) store_quarter(r0, NT, px, s_bias, L.Cout, res, y, L.v32 != 0);
-                if (position(1, &px)) store_quarter(r1, NT, px, s_bias, L.Cout, res, y, L.v32 != 0);
+                if (position(0, &px)) store_quarter(r0, NT, 0, px, s_bias, L.Cout, res, y, L.v32 != 0);
+                if (position(1, &px)) store_quarter(r1, NT, 0, px, s_bias, L.Cout, res, y, L.v32 != 0);
             }
         }
     }

@@ -216,6 +216,76 @@ __device__ __forceinline__ void copy_history(const TcLaunch& L, int P, int cw, i
     }
 }
 
+// Epilogues that hand accumulators back before touching memory: read NT <= 96 columns of this
+// thread's lane into registers (tmem_read_quarter, then tmem_ld_wait), optionally zero them
+// (tmem_zero_quarter, then tmem_st_wait), release them, and only then add bias / residual and
+// store (store_quarter): the MMA warps wait for tensor-memory reads only, never for memory.
+__device__ __forceinline__ void tmem_read_quarter(uint32_t tbase, int NT, uint32_t* r)
+{
+#pragma unroll
+    for (int g = 0; g < 3; ++g) {
+        if (g * 32 + 32 <= NT)
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(g * 32), r + g * 32);
+        else if (g * 32 + 16 == NT)
+            tmem_ld_32x32b_x16(tbase + (uint32_t)(g * 32), r + g * 32);
+    }
+}
+
+__device__ __forceinline__ void tmem_zero_quarter(uint32_t tbase, int NT)
+{
+#pragma unroll
+    for (int g = 0; g < 3; ++g) {
+        if (g * 32 + 32 <= NT)
+            tmem_st_32x32b_x32_zero(tbase + (uint32_t)(g * 32));
+        else if (g * 32 + 16 == NT)
+            tmem_st_32x32b_x16_zero(tbase + (uint32_t)(g * 32));
+    }
+}
+
+// bias (+ residual) and the bf16 stores of NT <= 96 accumulator columns held in registers, output
+// channels co0 .. co0 + NT - 1 of position px, 32 columns at a time; with `v32` every 16 channels
+// move as one 32-byte load / store
+__device__ __forceinline__ void store_quarter(const uint32_t* r, int NT, int co0, size_t px, const float* s_bias,
+                                              int Cout, const __nv_bfloat16* res, __nv_bfloat16* y, bool v32)
+{
+    __nv_bfloat16* yp = y + px * Cout + co0;
+    const __nv_bfloat16* rq = res + px * Cout + co0;
+    if (v32) {
+#pragma unroll
+        for (int g = 0; g < 3; ++g) {
+            if (g * 32 + 16 > NT) break;
+            const bool two = g * 32 + 32 <= NT;
+            if (res != nullptr) {
+                uint32_t rr[16];
+                ld_nc_v8(rq + g * 32, rr);
+                if (two) ld_nc_v8(rq + g * 32 + 16, rr + 8);
+                store16_v8<true>(r + g * 32, s_bias, co0 + g * 32, yp + g * 32, rr);
+                if (two) store16_v8<true>(r + g * 32 + 16, s_bias, co0 + g * 32 + 16, yp + g * 32 + 16, rr + 8);
+            } else {
+                store16_v8<false>(r + g * 32, s_bias, co0 + g * 32, yp + g * 32, nullptr);
+                if (two) store16_v8<false>(r + g * 32 + 16, s_bias, co0 + g * 32 + 16, yp + g * 32 + 16, nullptr);
+            }
+        }
+        return;
+    }
+    const uint4* rp = reinterpret_cast<const uint4*>(rq);
+#pragma unroll
+    for (int g = 0; g < 3; ++g) {
+        if (g * 32 + 16 > NT) break;
+        const bool two = g * 32 + 32 <= NT;
+        if (res != nullptr) {
+            uint4 rv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) rv[k] = (k < 2 || two) ? __ldg(rp + 4 * g + k) : make_uint4(0, 0, 0, 0);
+            store16_res(r + g * 32, s_bias, co0 + g * 32, yp + g * 32, rv[0], rv[1]);
+            if (two) store16_res(r + g * 32 + 16, s_bias, co0 + g * 32 + 16, yp + g * 32 + 16, rv[2], rv[3]);
+        } else {
+            store16(r + g * 32, s_bias, co0 + g * 32, px, Cout, true, nullptr, y);
+            if (two) store16(r + g * 32 + 16, s_bias, co0 + g * 32 + 16, px, Cout, true, nullptr, y);
+        }
+    }
+}
+
 // the epilogue warp is done reading this accumulator stage: let the MMA warps overwrite it
 __device__ __forceinline__ void release_acc(uint64_t* bar, int lane)
 {

@@ -80,6 +80,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
     const unsigned long long budget = L.wait_ns;
     const int KSZ = L.ks;     // spatial kernel extent (kh = kw): 3, or 1 for temporal / pointwise kernels
     const int P = L.kt - 1;   // history frames in the cache
+    // one accumulator buffer shared by two MMA warps that own disjoint 128-row groups (or
+    // output classes): each warp waits only for its own part to be drained
+    const bool per_warp_release = L.acc_stages == 1 && nissue == 2 && !L.split_n;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -87,9 +90,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         for (int s = 0; s < L.na; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], nissue); }
         for (int s = 0; s < L.nb; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], nissue); }
         for (int a = 0; a < L.acc_stages; ++a) mbar_init(&acc_full[a], nissue);
-        // released by the 4 epilogue warps; an upsampling layer (one accumulator stage) releases
-        // the two MMA warps' class pairs separately, on acc_empty[0] and acc_empty[1]
-        for (int a = 0; a < (L.up2 ? 2 : L.acc_stages); ++a) mbar_init(&acc_empty[a], 4);
+        // released by the 4 epilogue warps; with one accumulator stage and two MMA warps that
+        // split the rows (or an upsampling layer's classes), each MMA warp's part is released
+        // separately, on acc_empty[0] and acc_empty[1]
+        for (int a = 0; a < (per_warp_release ? 2 : L.acc_stages); ++a) mbar_init(&acc_empty[a], 4);
         mbar_init(&mma_drain[0], 1);
         mbar_init(&mma_drain[1], 1);
         fence_mbar_init();
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             const TileCoord c = tile_coord(L, tile);
             const int as = it % L.acc_stages;
             const int aph = (it / L.acc_stages) & 1;
-            if (!warp_bounded_wait(&acc_empty[L.up2 ? k : as], aph ^ 1, budget, &abort_flag)) {
+            if (!warp_bounded_wait(&acc_empty[per_warp_release ? k : as], aph ^ 1, budget, &abort_flag)) {
                 if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
                 break;
             }
@@ -380,10 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                         if (NT <= 96 && wide) {
                             for (int u = 0; u < 2; ++u) {
                                 uint32_t r[96];
-                                tmem_read_quarter(tb + (uint32_t)(u * NT), NT, r);
+                                tmem_read_quarter<96>(tb + (uint32_t)(u * NT), NT, r);
                                 tmem_ld_wait();
                                 if (last_m && u == 1) release_acc(&acc_empty[kp], lane);
-                                if (valid) store_quarter(r, NT, c.co0, out_px(u), s_bias, L.Cout, res, y, L.v32 != 0);
+                                if (valid) store_quarter<96>(r, NT, c.co0, out_px(u), s_bias, L.Cout, res, y, L.v32 != 0);
                             }
                         } else {
                             for (int u = 0; u < 2; ++u)
@@ -402,6 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                 const int w = c.w0 + jcol - 1;
                 const bool valid = h < L.H && jcol >= 1 && jcol <= L.g.S && w < L.W;
                 const size_t px = ((size_t)c.t * L.H + (valid ? h : 0)) * L.W + (valid ? w : 0);
+                if (per_warp_release) {
+                    // row group m belongs to MMA warp m / SUBI; the read of its last row group of
+                    // the tile releases that warp's part (the other warp's part may still be
+                    // waiting for the epilogue)
+                    const int owner = m / SUBI;
+                    const bool last_of_owner = (m % SUBI) == SUBI - 1;
+                    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * nsplit * NT);
+                    for (int ns = 0; ns < nsplit; ++ns)
+                        epilogue_slice(tbase + (uint32_t)(ns * NT), NT, c.co0 + ns * NT, px, valid,
+                                       last_of_owner && ns == nsplit - 1, s_bias, L.Cout, wide, res, y, L.v32 != 0,
+                                       [&]() { release_acc(&acc_empty[owner], lane); });
+                    continue;
+                }
                 for (int ns = 0; ns < nsplit; ++ns) {
                     const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +
                                            (uint32_t)((m * nsplit + ns) * NT);

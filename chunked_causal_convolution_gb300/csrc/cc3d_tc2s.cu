@@ -360,19 +360,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2s, 1)
                 uint32_t r0[96], r1[96];
                 const uint32_t tb0 = lane_base + (uint32_t)(half * NT);
                 const uint32_t tb1 = tb0 + (uint32_t)(2 * NT);
-                tmem_read_quarter(tb0, NT, r0);
-                tmem_read_quarter(tb1, NT, r1);
+                tmem_read_quarter<96>(tb0, NT, r0);
+                tmem_read_quarter<96>(tb1, NT, r1);
                 tmem_ld_wait();
                 if (half == 1) {
-                    tmem_zero_quarter(tb0, NT);
-                    tmem_zero_quarter(tb1, NT);
+                    tmem_zero_quarter<96>(tb0, NT);
+                    tmem_zero_quarter<96>(tb1, NT);
                     tmem_st_wait();
                 }
                 release_to(half == 0 ? &accA_empty[0] : &accB_empty[0]);
                 release_to(half == 0 ? &accA_empty[1] : &accB_empty[1]);
                 size_t px;
-                if (position(0, &px)) store_quarter(r0, NT, 0, px, s_bias, L.Cout, res, y, L.v32 != 0);
-                if (position(1, &px)) store_quarter(r1, NT, 0, px, s_bias, L.Cout, res, y, L.v32 != 0);
+                if (position(0, &px)) store_quarter<96>(r0, NT, 0, px, s_bias, L.Cout, res, y, L.v32 != 0);
+                if (position(1, &px)) store_quarter<96>(r1, NT, 0, px, s_bias, L.Cout, res, y, L.v32 != 0);
             }
         }
     }

@@ -216,14 +216,15 @@ __device__ __forceinline__ void copy_history(const TcLaunch& L, int P, int cw, i
     }
 }
 
-// Epilogues that hand accumulators back before touching memory: read NT <= 96 columns of this
+// Epilogues that hand accumulators back before touching memory: read NT <= MAXC columns of this
 // thread's lane into registers (tmem_read_quarter, then tmem_ld_wait), optionally zero them
 // (tmem_zero_quarter, then tmem_st_wait), release them, and only then add bias / residual and
 // store (store_quarter): the MMA warps wait for tensor-memory reads only, never for memory.
+template <int MAXC>
 __device__ __forceinline__ void tmem_read_quarter(uint32_t tbase, int NT, uint32_t* r)
 {
 #pragma unroll
-    for (int g = 0; g < 3; ++g) {
+    for (int g = 0; g < MAXC / 32; ++g) {
         if (g * 32 + 32 <= NT)
             tmem_ld_32x32b_x32(tbase + (uint32_t)(g * 32), r + g * 32);
         else if (g * 32 + 16 == NT)
@@ -231,10 +232,11 @@ __device__ __forceinline__ void tmem_read_quarter(uint32_t tbase, int NT, uint32
     }
 }
 
+template <int MAXC>
 __device__ __forceinline__ void tmem_zero_quarter(uint32_t tbase, int NT)
 {
 #pragma unroll
-    for (int g = 0; g < 3; ++g) {
+    for (int g = 0; g < MAXC / 32; ++g) {
         if (g * 32 + 32 <= NT)
             tmem_st_32x32b_x32_zero(tbase + (uint32_t)(g * 32));
         else if (g * 32 + 16 == NT)
@@ -242,9 +244,10 @@ __device__ __forceinline__ void tmem_zero_quarter(uint32_t tbase, int NT)
     }
 }
 
-// bias (+ residual) and the bf16 stores of NT <= 96 accumulator columns held in registers, output
+// bias (+ residual) and the bf16 stores of NT <= MAXC accumulator columns held in registers, output
 // channels co0 .. co0 + NT - 1 of position px, 32 columns at a time; with `v32` every 16 channels
 // move as one 32-byte load / store
+template <int MAXC>
 __device__ __forceinline__ void store_quarter(const uint32_t* r, int NT, int co0, size_t px, const float* s_bias,
                                               int Cout, const __nv_bfloat16* res, __nv_bfloat16* y, bool v32)
 {
@@ -252,7 +255,7 @@ __device__ __forceinline__ void store_quarter(const uint32_t* r, int NT, int co0
     const __nv_bfloat16* rq = res + px * Cout + co0;
     if (v32) {
 #pragma unroll
-        for (int g = 0; g < 3; ++g) {
+        for (int g = 0; g < MAXC / 32; ++g) {
             if (g * 32 + 16 > NT) break;
             const bool two = g * 32 + 32 <= NT;
             if (res != nullptr) {
@@ -270,7 +273,7 @@ __device__ __forceinline__ void store_quarter(const uint32_t* r, int NT, int co0
     }
     const uint4* rp = reinterpret_cast<const uint4*>(rq);
 #pragma unroll
-    for (int g = 0; g < 3; ++g) {
+    for (int g = 0; g < MAXC / 32; ++g) {
         if (g * 32 + 16 > NT) break;
         const bool two = g * 32 + 32 <= NT;
         if (res != nullptr) {

@@ -204,9 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         const int m0 = (L.split_n || L.up2) ? 0 : k * SUBI;
         // upsampling layers: four output classes per row group, two per MMA warp
         const int ncls = L.up2 ? 4 : 1;
-        const int cls_lo = L.up2 ? 2 * k : 0, cls_hi = L.up2 ? 2 * k + 2 : 1;
         const int ns_lo = L.split_n ? k : 0, ns_hi = L.split_n ? k + 1 : nsplit;
         const uint32_t idesc = make_idesc_bf16_f32(128, NT);
+        const uint32_t idesc2 = make_idesc_bf16_f32(128, L.up2 ? 2 * NT : NT);  // two classes side by side
         const uint64_t a_desc0 = make_sdesc(smem_u32(smA), 16, SBO, LAYOUT, 0);
         const uint64_t b_desc0 = make_sdesc(smem_u32(smB), 16, SBO, LAYOUT, 0);
         const uint32_t a_inc = (uint32_t)L.a_stage_bytes >> 4;
@@ -253,26 +253,53 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                             const uint32_t dcol = dbase + (uint32_t)(ns * NT) + (uint32_t)m0 * m_cols;
                             const bool mine = ns >= ns_lo && ns < ns_hi;
                             if (L.up2) {
-                                // output class (a, b) of source position (i, j) is the upsampled
+                                // Output class (a, b) of source position (i, j) is the upsampled
                                 // pixel (2i + a, 2j + b): its tap (dh, dw) reads source pixel
                                 // (i + floor((a + dh - 1) / 2), j + floor((b + dw - 1) / 2)), a view
-                                // of the same window shifted by 0..2 rows and 0..2 pixels
+                                // of the same window shifted by 0..2 rows and 0..2 pixels.  MMA
+                                // warp k owns class row a = k; its two classes (slots 2a: b = 1,
+                                // 2a + 1: b = 0, in that column order) read the same view for
+                                // taps (dw = 0 of b = 1, dw = 1 of b = 0) and (dw = 1 of b = 1,
+                                // dw = 2 of b = 0), whose weight taps lie side by side in the
+                                // stage: those pairs go through one MMA with N = 2 NT.  Per tap row:
+                                //   b = 0, dw = 0 (view 0)   N = NT
+                                //   both, dw = 0 | 1 (view 1) N = 2 NT
+                                //   both, dw = 1 | 2 (view 1) N = 2 NT
+                                //   b = 1, dw = 2 (view 2)   N = NT
+                                // which keeps each class's order dh, dw, 16-channel step.  The
+                                // first stacked MMA of a tile is issued as its two halves, so that
+                                // class (a, 1) starts from zero while (a, 0) accumulates.
+                                const int a = k;
+                                const uint32_t slot1 = dcol + (uint32_t)(2 * a * NT);  // class (a, 1), then (a, 0)
+                                const uint32_t slot0 = slot1 + (uint32_t)NT;
                                 for (int dr = 0; dr < RB; ++dr) {
                                     const int dh = dg * RB + dr;
                                     const bool first_row = (dt | cb | dh) == 0;
-                                    for (int dw = 0; dw < 3; ++dw) {
-                                        for (int cls = cls_lo; cls < cls_hi; ++cls) {
-                                            const int sh1 = ((cls >> 1) + dh + 1) >> 1, sw1 = ((cls & 1) + dw + 1) >> 1;
-                                            const uint64_t view = desc_add(a_st, sh1 * row_shift + sw1 * ROWU);
-                                            const uint32_t dcls = dcol + (uint32_t)(cls * NT);
+                                    const uint64_t vrow = desc_add(a_st, ((a + dh + 1) >> 1) * row_shift);
+                                    const uint64_t btap = desc_add(b_st, (dr * 3) * b_tap_inc);
 #pragma unroll
-                                            for (int m = 0; m < SUBI; ++m) {
+                                    for (int m = 0; m < SUBI; ++m) {
 #pragma unroll
-                                                for (int ks = 0; ks < KSTEPS; ++ks) {
-                                                    const uint64_t ad = desc_add(view, rowu[m] + ks * 2);
-                                                    const uint64_t bd = desc_add(b_st, (dr * 3 + dw) * b_tap_inc + ks * 2);
-                                                    const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
-                                                    if (lead) umma_bf16_ss(dcls + (uint32_t)m * m_cols, ad, bd, idesc, acc);
+                                        for (int kind = 0; kind < 4; ++kind) {
+                                            const int sw1 = kind == 0 ? 0 : (kind == 3 ? 2 : 1);
+                                            const int dw0 = kind == 0 ? 0 : (kind == 3 ? 2 : kind - 1);  // first weight tap
+                                            const uint32_t dst = (kind == 0 ? slot0 : slot1) + (uint32_t)m * m_cols;
+#pragma unroll
+                                            for (int ks = 0; ks < KSTEPS; ++ks) {
+                                                const uint64_t ad = desc_add(vrow, sw1 * ROWU + rowu[m] + ks * 2);
+                                                const uint64_t bd = desc_add(btap, dw0 * b_tap_inc + ks * 2);
+                                                if (kind == 1 || kind == 2) {
+                                                    if (kind == 1 && first_row && ks == 0) {
+                                                        // halves: (a, 1) tap dw = 0 from zero, (a, 0) tap dw = 1
+                                                        if (lead) umma_bf16_ss(dst, ad, bd, idesc, 0u);
+                                                        if (lead)
+                                                            umma_bf16_ss(dst + (uint32_t)NT, ad, desc_add(bd, b_tap_inc), idesc, 1u);
+                                                    } else if (lead) {
+                                                        umma_bf16_ss(dst, ad, bd, idesc2, 1u);
+                                                    }
+                                                } else {
+                                                    const uint32_t acc = (kind == 0 && first_row && ks == 0) ? 0u : 1u;
+                                                    if (lead) umma_bf16_ss(dst, ad, bd, idesc, acc);
                                                 }
                                             }
                                         }
@@ -372,11 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                         const int w = c.w0 + jcol - 1;
                         const bool valid = h < L.H && jcol >= 1 && jcol <= L.g.S && w < L.W;
                         const bool last_m = m == SUB - 1;
-                        // output position of class 2 kp + u of this lane's source pixel
+                        // output position of the class in column slot 2 kp + u: class (kp, 1 - u)
                         auto out_px = [&](int u) {
-                            const int cls = 2 * kp + u;
-                            const size_t oh = valid ? 2 * (size_t)h + (cls >> 1) : 0;
-                            const size_t ow = valid ? 2 * (size_t)w + (cls & 1) : 0;
+                            const size_t oh = valid ? 2 * (size_t)h + kp : 0;
+                            const size_t ow = valid ? 2 * (size_t)w + (1 - u) : 0;
                             return ((size_t)c.t * 2 * L.H + oh) * 2 * L.W + ow;
                         };
                         const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * acc_cols +

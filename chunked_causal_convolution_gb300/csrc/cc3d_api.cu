@@ -625,11 +625,25 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
     L.fault = p.fault;
     // tiles: one per output frame, or per pair of output frames in the two-frame schedule
     const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * (L.tstack ? (T + 1) / 2 : T) * L.ncoblk;
+    L.nfull = ntiles;
+    L.nunits = ntiles;
     if (L.pair) {
         const int npairs = (ntiles + 1) / 2;
         L.grid = 2 * (npairs < d->sms / 2 ? npairs : d->sms / 2);
     } else {
-        L.grid = ntiles < d->sms ? ntiles : d->sms;
+        // A short last wave (at most half the SMs busy) of two-row-group tiles with one
+        // accumulator buffer: split those tiles into one-row-group units, each computed by both
+        // MMA warps on half of the output channels, so every block gets about the same work
+        // (c384 -> 192 at 90 x 160: 228 tiles = 152 whole + 76 split over 152 SMs).
+        const char* env = getenv("CC3D_TC_SPLIT");
+        const bool allow = env == nullptr || *env == 0 || atoi(env) != 0;
+        const int R = ntiles % d->sms;
+        if (allow && L.acc_stages == 1 && L.issuers == 2 && !L.split_n && !L.up2 && L.nsplit == 1 &&
+            L.g.sub == 2 && L.NT % 32 == 0 && R > 0 && 2 * R <= d->sms) {
+            L.nfull = ntiles - R;
+            L.nunits = L.nfull + 2 * R;
+        }
+        L.grid = L.nunits < d->sms ? L.nunits : d->sms;
     }
     // ---- the new history: cache_out slot j = frame T + j of the stack (cache_in frames, then x
     // frames; zeros for a missing cache_in), moved by the copy engines while the kernel runs

@@ -54,6 +54,11 @@ struct TcLaunch {
     int rb;                           // kernel rows (of ks taps) per B stage: 1 or 3 (1 when ks == 1)
     int pair;                         // 1: SM-pair kernel (cta_group::2), weight rows split in two
     int tstack;                       // 1: SM pairs with two output frames stacked into N per MMA
+    // one-SM kernel work units: units [0, nfull) are whole tiles; the rest split tiles nfull, ...
+    // into their two 128-row groups, two units per tile, each computed by both MMA warps (one half
+    // of the output channels each), so that a short last wave spreads over all blocks (nunits =
+    // tiles when nothing is split)
+    int nfull, nunits;
     int v32;                          // y and the residual are 32-byte aligned: 32-byte epilogue accesses
     int split_n;                      // with 2 issuers: split by N slice (else by 128-row group)
     int a_stage_bytes, b_stage_bytes;

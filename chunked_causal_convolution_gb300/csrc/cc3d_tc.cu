@@ -47,6 +47,18 @@ using namespace tcc;
 
 namespace {
 
+// Work unit u of the one-SM kernel: its tile, and the mask of its 128-row groups (bit m: row
+// group m of the tile; a split tile's two units hold one row group each).
+__device__ __forceinline__ int unit_tile(const TcLaunch& L, int u)
+{
+    return u < L.nfull ? u : L.nfull + ((u - L.nfull) >> 1);
+}
+
+__device__ __forceinline__ int unit_mask(const TcLaunch& L, int u)
+{
+    return u < L.nfull ? 0xF : 1 << ((u - L.nfull) & 1);
+}
+
 template <int CB, int SUBI, int RB>
 __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_constant__ TcLaunch L)
 {
@@ -72,7 +84,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
     const int NT = L.NT;
     const int nsplit = L.nsplit;
     const int ncb = L.Cin / CB;
-    const int ntiles = L.g.tiles_per_cb * L.g.ncolblk * L.T * L.ncoblk;
     const int cout_pad = L.ncoblk * nsplit * NT;
     const int SUB = L.g.sub;                   // 128-row groups per tile (all MMA warps together)
     const int nissue = L.issuers;              // MMA-issuing warps (1 or 2)
@@ -127,12 +138,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
             const uint32_t b_tx = (uint32_t)(ROWB * NT * KSZ * RB);
             bool skip_first = (L.fault == 1);
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-                const TileCoord c = tile_coord(L, tile);
+            for (int u = blockIdx.x; ok && u < L.nunits; u += gridDim.x) {
+                const TileCoord c = tile_coord(L, unit_tile(L, u));
                 // optionally warm L2 with the input windows of this block's next tile
-                const int next = tile + (int)gridDim.x;
-                if (L.prefetch && next < ntiles) {
-                    const TileCoord n = tile_coord(L, next);
+                const int next = u + (int)gridDim.x;
+                if (L.prefetch && next < L.nunits) {
+                    const TileCoord n = tile_coord(L, unit_tile(L, next));
                     for (int dt = L.kt > L.prefetch ? L.kt - L.prefetch : 0; dt < L.kt; ++dt) {
                         const int tin = n.t + dt - P;
                         const bool from_cache = tin < 0 && L.has_cache;
@@ -206,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         const int ncls = L.up2 ? 4 : 1;
         const int ns_lo = L.split_n ? k : 0, ns_hi = L.split_n ? k + 1 : nsplit;
         const uint32_t idesc = make_idesc_bf16_f32(128, NT);
+        const uint32_t idesc_h = make_idesc_bf16_f32(128, NT >= 32 ? NT / 2 : NT);  // split tiles: half of N
         const uint32_t idesc2 = make_idesc_bf16_f32(128, L.up2 ? 2 * NT : NT);  // two classes side by side
         const uint64_t a_desc0 = make_sdesc(smem_u32(smA), 16, SBO, LAYOUT, 0);
         const uint64_t b_desc0 = make_sdesc(smem_u32(smB), 16, SBO, LAYOUT, 0);
@@ -217,21 +229,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         int sa = 0, pa = 0, sb = 0, pb = 0;
         bool ok = true;
         int it = 0;
-        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
-            const TileCoord c = tile_coord(L, tile);
+        for (int u = blockIdx.x; ok && u < L.nunits; u += gridDim.x, ++it) {
+            const TileCoord c = tile_coord(L, unit_tile(L, u));
+            const int umask = unit_mask(L, u);
+            // a split tile's unit: one row group (hrg), whose output channels the two MMA warps
+            // share, NT / 2 each (each output's accumulation order is unchanged)
+            const bool half = umask != 0xF;
+            const int hrg = umask >> 1;
             const int as = it % L.acc_stages;
             const int aph = (it / L.acc_stages) & 1;
-            if (!warp_bounded_wait(&acc_empty[per_warp_release ? k : as], aph ^ 1, budget, &abort_flag)) {
+            bool freed = warp_bounded_wait(&acc_empty[per_warp_release ? k : as], aph ^ 1, budget, &abort_flag);
+            if (freed && half) freed = warp_bounded_wait(&acc_empty[1 - k], aph ^ 1, budget, &abort_flag);
+            if (!freed) {
                 if (lane == 0 && !abort_flag) record_failure(L, STATUS_TIMEOUT_MMA, &abort_flag);
                 break;
             }
             tc_fence_after();
             const uint32_t dbase = tmem + (uint32_t)as * acc_cols;
+            const int mrow = half ? hrg : m0;  // first row group this warp issues
+            const uint32_t hcol = half ? (uint32_t)(k * (NT / 2)) : 0u;  // its columns / weight rows
+            const uint32_t idesc_u = half ? idesc_h : idesc;
             // window row of the (dh = 0, dw = 0) view of each 128-row group, in descriptor units
             uint32_t rowu[SUBI];
 #pragma unroll
             for (int m = 0; m < SUBI; ++m)
-                rowu[m] = (uint32_t)(c.f0 + (m0 + m) * L.g.sub_stride - c.hstart * Sp - L.g.halo * (Sp + 1)) * ROWU;
+                rowu[m] = (uint32_t)(c.f0 + (mrow + m) * L.g.sub_stride - c.hstart * Sp - L.g.halo * (Sp + 1)) * ROWU;
             for (int dt = 0; ok && dt < L.kt; ++dt) {
                 for (int cb = 0; ok && cb < ncb; ++cb) {
                     if (!warp_bounded_wait(&a_full[sa], pa, budget, &abort_flag)) {
@@ -250,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                             }
                             tc_fence_after();
                             const uint64_t b_st = b_desc0 + (uint64_t)(sb * b_inc);
-                            const uint32_t dcol = dbase + (uint32_t)(ns * NT) + (uint32_t)m0 * m_cols;
+                            const uint32_t dcol = dbase + (uint32_t)(ns * NT) + (uint32_t)mrow * m_cols + hcol;
                             const bool mine = ns >= ns_lo && ns < ns_hi;
                             if (L.up2) {
                                 // Output class (a, b) of source position (i, j) is the upsampled
@@ -319,10 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
 #pragma unroll
                                         for (int ks = 0; ks < KSTEPS; ++ks) {
                                             const uint64_t ad = desc_add(a_row, rowu[m] + dw * ROWU + ks * 2);
-                                            const uint64_t bd = desc_add(b_st, (dr * KSZ + dw) * b_tap_inc + ks * 2);
+                                            const uint64_t bd =
+                                                desc_add(b_st, (dr * KSZ + dw) * b_tap_inc + hcol * ROWU + ks * 2);
                                             const uint32_t acc = (first_row && dw == 0 && ks == 0) ? 0u : 1u;
                                             if (mine && lead)
-                                                umma_bf16_ss(dcol + (uint32_t)m * m_cols, ad, bd, idesc, acc);
+                                                umma_bf16_ss(dcol + (uint32_t)m * m_cols, ad, bd, idesc_u, acc);
                                         }
                                     }
                                 }
@@ -358,10 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
         __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(L.y);
         const bool wide = (L.Cout % 16) == 0;
         int it = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+        for (int u = blockIdx.x; u < L.nunits; u += gridDim.x, ++it) {
+            const int umask = unit_mask(L, u);  // row groups of this unit (all of a whole tile)
+            const bool half = umask != 0xF;
+            const int hrg = umask >> 1;
             const int as = it % L.acc_stages;
             const int aph = (it / L.acc_stages) & 1;
-            const TileCoord c = tile_coord(L, tile);
+            const TileCoord c = tile_coord(L, unit_tile(L, u));
             // while the accumulators fill, pull this thread's residual lines into L2
             if (res != nullptr && wide && !L.up2) {
                 for (int m = 0; m < SUB; ++m) {
@@ -432,6 +458,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
                 const int w = c.w0 + jcol - 1;
                 const bool valid = h < L.H && jcol >= 1 && jcol <= L.g.S && w < L.W;
                 const size_t px = ((size_t)c.t * L.H + (valid ? h : 0)) * L.W + (valid ? w : 0);
+                if (per_warp_release && half) {
+                    // a split tile's unit: only row group hrg, written by both MMA warps, which
+                    // both wait for both releases
+                    if (m != hrg) continue;
+                    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * nsplit * NT);
+                    epilogue_slice(tbase, NT, c.co0, px, valid, true, s_bias, L.Cout, wide, res, y, L.v32 != 0,
+                                   [&]() {
+                                       release_acc(&acc_empty[0], lane);
+                                       release_acc(&acc_empty[1], lane);
+                                   });
+                    continue;
+                }
                 if (per_warp_release) {
                     // row group m belongs to MMA warp m / SUBI; the read of its last row group of
                     // the tile releases that warp's part (the other warp's part may still be

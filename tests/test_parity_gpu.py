@@ -579,3 +579,29 @@ def test_outputs_and_residual_only_16_byte_aligned(case):
     assert plan.status() == 0
     assert torch.equal(y16, y_ref)
     plan.close()
+
+
+@pytest.mark.parametrize("shape", [(192, 192, 5, 6, 64), (384, 192, 4, 5, 40), (64, 256, 3, 7, 100)],
+                         ids=["c192_like", "c384_to_192_like", "c64_to_256"])
+def test_split_tail_tiles_are_bit_identical(shape, monkeypatch):
+    """A short last wave of two-row-group tiles is split into one-row-group units that both MMA
+    warps compute, on half of the output channels each (at these sizes every tile is split).
+    Each output keeps its MMAs and their order, so the result equals the unsplit launch bit for
+    bit, and the oracle within tolerance."""
+    Cin, Cout, T, H, W = shape
+    raw = small_inputs(Cin, Cout, T, H, W, "bf16", 400 + Cin, True, True)
+    dev = {kk: to_device(v, "bf16") for kk, v in raw.items()}
+    plan = cc3d.CausalConv3dPlan(Cin, Cout, H, W)
+    assert plan.kernel == "tc_bf16"
+    y_split, c_split = run_chunks(plan, dev["x"], dev["w"], dev["b"], dev["r"], [T - 1, 1])
+    assert plan.status() == 0
+    monkeypatch.setenv("CC3D_TC_SPLIT", "0")
+    y_whole, c_whole = run_chunks(plan, dev["x"], dev["w"], dev["b"], dev["r"], [T - 1, 1])
+    assert plan.status() == 0
+    monkeypatch.delenv("CC3D_TC_SPLIT")
+    assert torch.equal(y_split, y_whole)
+    assert all(torch.equal(a, b) for a, b in zip(c_split, c_whole))
+    ref = oracle.conv_whole(to_f64(raw["x"], "bf16"), to_f64(raw["w"], "bf16"), to_f64(raw["b"], "bf16"),
+                            to_f64(raw["r"], "bf16"))
+    assert np.abs(from_device(y_split) - ref).max() <= tolerance("bf16", ref)
+    plan.close()

@@ -50,6 +50,9 @@
  *  - Kernel waits are bounded.  A wait that runs out records an error in a
  *    per-device status word and the kernel returns; cc3d_get_status reports
  *    it.
+ *  - A plan is used from one host thread at a time (its side stream and
+ *    events, see cc3d_forward_chunk, are per plan); different plans may be
+ *    used from different threads concurrently.
  */
 #ifndef CC3D_H
 #define CC3D_H

@@ -604,19 +604,24 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
     // geometry) and the same weights (one output-channel block); then each block holds half of
     // every weight stage and the tensor core reads less shared memory per MMA.  Two row groups
     // per block with double-buffered accumulators, measured best for narrow layers.
+    // Tiles are ordered frame fastest, so with an even number of frames the two tiles of a pair
+    // are consecutive frames at one spatial position (and one output-channel block): they share
+    // window offsets and weights in any geometry.  With an odd number the row-aligned geometry
+    // (W a multiple of 128, equal offsets everywhere) still pairs a single channel block.
     L->pair = 0;
-    if (!up2 && W % 128 == 0 && L->ncoblk == 1 && L->nsplit == 1 && L->NT >= 32 && L->NT <= 128 &&
-        env_int("CC3D_TC_PAIR", 1)) {
+    const bool pair_tiles_match = T % 2 == 0 || (W % 128 == 0 && L->ncoblk == 1);
+    if (!up2 && pair_tiles_match && L->nsplit == 1 && L->NT >= 32 && L->NT <= 192 && env_int("CC3D_TC_PAIR", 1)) {
         L->pair = 1;
         sub = env_int("CC3D_TC_SUB", 2);
-        acc = env_int("CC3D_TC_ACC", 2);
+        acc = env_int("CC3D_TC_ACC", 2 * 2 * L->NT <= 512 ? 2 : 1);
     }
     // two output frames per pair tile, stacked into N where an input frame is a tap of both
     // (chunks of two or more frames of a kt x 3 x 3 kernel with kt >= 2, up to 96 output channels;
     // with kt = 2 one of three input frames is shared, measured 1 % faster): two row groups per
     // block, one accumulator buffer of 2 frames x 2 row groups x NT columns
     L->tstack = 0;
-    if (L->pair && kt >= 2 && ks == 3 && T >= 2 && L->NT <= 96 && sub_cap >= 2 && env_int("CC3D_TC_TSTACK", 1)) {
+    if (L->pair && W % 128 == 0 && L->ncoblk == 1 && kt >= 2 && ks == 3 && T >= 2 && L->NT <= 96 && sub_cap >= 2 &&
+        env_int("CC3D_TC_TSTACK", 1)) {
         L->tstack = 1;
         sub = 2;
         acc = 1;
@@ -680,7 +685,10 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
     if (L->rb != 1 && L->rb != 3) return false;
     // weight rows of one block (the two-frame schedule's stacked stages hold a whole tap)
     const int b_rows = L->pair && !L->tstack ? L->NT / 2 : L->NT;
-    if (L->pair) L->rb = env_int("CC3D_TC_RB", ks == 3 ? 3 : 1);
+    // pairs: 9-tap weight stages in the row-aligned geometry (c96), 3-tap ones in the flat
+    // geometry, whose wide windows leave room for only two 9-tap stages (the weight ring was the
+    // wait there: c384 1960 against 1837 TFLOP/s)
+    if (L->pair) L->rb = env_int("CC3D_TC_RB", ks == 3 && W % 128 == 0 ? 3 : 1);
     if (L->tstack) L->rb = env_int("CC3D_TC_RB", 3);  // 9-tap stages: measured 8 % faster than 3-tap on c96
     if ((L->rb != 1 && L->rb != 3) || ks % L->rb != 0) return false;
     L->b_stage_bytes = (ks * L->rb * b_rows * rowb + 1023) & ~1023;

@@ -14,9 +14,12 @@
 // Per block and 128x96x16 step the tensor core reads 4 KB of activations and 1.5 KB of weights
 // from shared memory instead of 4 + 3 KB, and one issued instruction does twice the work.
 //
-// Requirement: both tiles of a pair must use the same window offsets, which holds when the
-// frame is cut into 128-pixel row segments (W a multiple of 128).  The host only selects this
-// kernel then.
+// Requirement: both tiles of a pair must use the same window offsets and weights.  Tiles are
+// ordered frame fastest, so with an even number of frames the pair's tiles are two frames at one
+// spatial position and output-channel block, in any geometry; with an odd number the host
+// selects this kernel only for one channel block in the row-aligned geometry (W a multiple of
+// 128), where every tile has the same offsets.  Up to 192 output channels per block (96 weight
+// rows in each block of the pair).
 #include <cuda_bf16.h>
 
 #include "cc3d_internal.h"

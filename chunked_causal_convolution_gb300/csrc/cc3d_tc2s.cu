@@ -343,10 +343,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2s, 1)
                     *px = ((size_t)(valid ? t : 0) * L.H + (valid ? h : 0)) * L.W + (valid ? w : 0);
                     return valid;
                 };
-                for (int m = 0; m < kSub; ++m) {
-                    size_t px;
-                    const bool valid = position(m, &px);
-                    prefetch_residual(res, px, L.Cout, valid);
+                // both frames' residual rows are warmed at the start of the tile: frame t + 1's
+                // are read right after its columns are released, too soon after frame t's stores
+                // for a prefetch issued there to have landed
+                if (half == 0) {
+                    for (int m = 0; m < kSub; ++m) {
+                        size_t px;
+                        const bool valid = position(m, &px);
+                        prefetch_residual(res, px, L.Cout, valid);
+                        prefetch_residual(res, px + (size_t)L.H * L.W, L.Cout, valid && t + 1 < L.T);
+                    }
                 }
                 int ready = 0;
                 if (lane == 0) {

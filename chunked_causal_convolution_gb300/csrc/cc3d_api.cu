@@ -117,12 +117,14 @@ struct cc3d_plan_s {
     int CB;
     unsigned long long wait_ns;
     int fault;
-    // The one-frame SM-pair kernel's new history is copied by a copy engine on a side stream,
-    // forked from the caller's stream before the launch and joined to it after (created on first
-    // use, on the device current then; on another device the kernel copies the history itself).
-    // Measured on GB300: 2x3x3 at 96 channels (one history frame) 1400 against 1315 TFLOP/s with
-    // the kernel's own copy warp; the other kernels are faster with their copy warp (a copy
-    // engine moves about 0.3 TB/s, and splitting the copy over more streams did not add to it).
+    // Part of the new history is copied by a copy engine on a side stream, forked from the
+    // caller's stream before the launch and joined to it after (created on first use, on the
+    // device current then; on another device the kernel copies the whole history itself): all of
+    // it for the one-frame SM-pair kernel, the first of the two frames for the two-frame kernel,
+    // none for the one-SM kernel.  Measured on GB300 against the kernel's own copy warp: 2x3x3 at
+    // 96 channels 1400 against 1315 TFLOP/s, 3x3x3 at 96 channels 1587 against 1558; the one-SM
+    // kernel lost 1.5-2.5 %.  A copy engine moves about 0.3 TB/s (more streams did not add to
+    // it), so a larger share outlasts the launch.
     static constexpr int kSide = 1;
     cudaStream_t side[kSide] = {};
     cudaEvent_t fork = nullptr;

@@ -12,7 +12,7 @@
 // and neighbouring rows (running sums kept in registers).  A block walks a contiguous run of rows
 // of one column strip (126 output pixels = 128 input positions with the halo), input row by input
 // row; every input row (all channels, the chunk's frames and the two history frames) is loaded
-// into shared memory once, and the copy engine writes the new history (the last two input frames)
+// into shared memory once, and TMA stores write the new history (the last two input frames)
 // back from there.  Rows are dealt out to the blocks in equal runs, so there is no tail wave.
 //
 // Accumulation order of one output (t, h, w, co), fixed whatever the chunking: inside the tensor
@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
         fence_mbar_init();
     }
     {
-        // weight rows 9 * COUT .. NCOL - 1 of every tile (the N padding) are zero; the copy engine
-        // fills the rows before them, so the two never touch the same bytes
+        // weight rows 9 * COUT .. NCOL - 1 of every tile (the N padding) are zero; the TMA loads
+        // fill the rows before them, so the two never touch the same bytes
         constexpr int pad16 = (NCOL - 9 * COUT) * ROWB / 16;
         const int ntiles = 3 * ncb;
         for (int i = threadIdx.x; i < ntiles * pad16; i += kThreads) {
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
         // ------------------------------------------------------------ temporal cache update
         // cache_out[k] is frame T - 2 + k of (cache_in or zeros) ++ x_chunk: the input frame that
         // the last frame group stages as j = G + k.  This warp follows the stage ring and has the
-        // copy engine store the interior of those stages (the segment's output rows; the strip's
+        // TMA unit store the interior of those stages (the segment's output rows; the strip's
         // 126 pixels, staged from row 8 on, a swizzle-atom boundary) to cache_out, so the history
         // is written from shared memory without a second read of x.
         int s = 0, ph = 0;

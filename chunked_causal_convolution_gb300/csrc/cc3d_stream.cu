@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
     } else if (warp == 3) {
         // ------------------------------------------------------------ temporal cache update
         // cache_out[k] is input frame T - P + k, which the last frame group stages as j = G + k:
-        // the copy engine stores those blocks straight from shared memory
+        // TMA stores write those blocks straight from shared memory
         if (P > 0) {
             int s = 0, ph = 0;
             bool ok = true;

@@ -27,8 +27,8 @@ __all__ = [
     "CC3D_F32", "CC3D_BF16", "CC3DError", "CausalConv3dPlan",
     "cc3d_plan_create", "cc3d_plan_create_upsample2x", "cc3d_forward_chunk", "cc3d_forward_chunk_u8",
     "cc3d_reset", "cc3d_get_status", "cc3d_destroy", "cc3d_status_string", "cc3d_plan_kernel",
-    "cc3d_plan_launches_per_chunk", "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault",
-    "cc3d_last_error_detail", "library_path", "Upsample2xConvPlan",
+    "cc3d_plan_launches_per_chunk", "cc3d_plan_describe", "cc3d_debug_set_wait_budget_ns",
+    "cc3d_debug_set_fault", "cc3d_last_error_detail", "library_path", "Upsample2xConvPlan",
     "load_library", "FrameWriter",
     "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
     "weights_from_torch_layout", "EXPORTED_SYMBOLS",
@@ -46,7 +46,7 @@ STATUS_NAMES = {
 EXPORTED_SYMBOLS = (
     "cc3d_plan_create", "cc3d_plan_create_upsample2x", "cc3d_forward_chunk", "cc3d_forward_chunk_u8", "cc3d_reset", "cc3d_get_status",
     "cc3d_destroy",
-    "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk",
+    "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk", "cc3d_plan_describe",
     "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_last_error_detail",
     "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
 )
@@ -95,6 +95,7 @@ def load_library():
         lib.cc3d_plan_kernel.argtypes = [vp]
         lib.cc3d_plan_kernel.restype = ctypes.c_char_p
         lib.cc3d_plan_launches_per_chunk.argtypes = [vp]
+        lib.cc3d_plan_describe.argtypes = [vp, i, i, ctypes.c_char_p, ctypes.c_size_t]
         lib.cc3d_debug_set_wait_budget_ns.argtypes = [vp, u64]
         lib.cc3d_debug_set_fault.argtypes = [vp, i]
         lib.cc3d_writer_create.argtypes = [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(vp)]
@@ -108,7 +109,7 @@ def load_library():
         lib.cc3d_last_error_detail.restype = ctypes.c_char_p
         for f in (lib.cc3d_plan_create, lib.cc3d_plan_create_upsample2x, lib.cc3d_forward_chunk, lib.cc3d_forward_chunk_u8, lib.cc3d_reset,
                   lib.cc3d_get_status,
-                  lib.cc3d_plan_launches_per_chunk, lib.cc3d_debug_set_wait_budget_ns,
+                  lib.cc3d_plan_launches_per_chunk, lib.cc3d_plan_describe, lib.cc3d_debug_set_wait_budget_ns,
                   lib.cc3d_debug_set_fault):
             f.restype = i
         _lib = lib
@@ -263,6 +264,18 @@ def cc3d_plan_launches_per_chunk(plan) -> int:
     return int(load_library().cc3d_plan_launches_per_chunk(plan))
 
 
+def cc3d_plan_describe(plan, T, has_residual=True) -> dict:
+    """The launch configuration of a T-frame chunk as {key: value} (ints where the value is one)."""
+    buf = ctypes.create_string_buffer(1024)
+    _check(load_library().cc3d_plan_describe(plan, int(T), 1 if has_residual else 0, buf, len(buf)),
+           "cc3d_plan_describe")
+    out = {}
+    for item in buf.value.decode().split():
+        k, v = item.split("=", 1)
+        out[k] = int(v) if v.lstrip("-").isdigit() else v
+    return out
+
+
 def cc3d_debug_set_wait_budget_ns(plan, ns: int):
     _check(load_library().cc3d_debug_set_wait_budget_ns(plan, int(ns)), "cc3d_debug_set_wait_budget_ns")
 
@@ -294,6 +307,10 @@ class CausalConv3dPlan:
     @property
     def launches_per_chunk(self) -> int:
         return cc3d_plan_launches_per_chunk(self.handle)
+
+    def describe(self, T, has_residual=True) -> dict:
+        """The launch configuration a T-frame chunk of this plan would use (host-only)."""
+        return cc3d_plan_describe(self.handle, T, has_residual)
 
     def torch_dtype(self):
         import torch

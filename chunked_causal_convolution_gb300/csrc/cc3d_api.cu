@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -418,6 +419,57 @@ int cc3d_plan_launches_per_chunk(cc3d_plan_t plan)
 {
     if (plan == nullptr) return 0;
     return plan->kind == K_SIMT_F32 ? 2 : 1;  // the tensor-core kernel also writes the new cache
+}
+
+cc3d_status cc3d_plan_describe(cc3d_plan_t plan, int T, int has_residual, char* buf, size_t len)
+{
+    if (plan == nullptr || buf == nullptr || len == 0 || T < 1) return CC3D_ERR_INVALID_ARG;
+    buf[0] = 0;
+    const cc3d_plan_s& p = *plan;
+    const int P = p.kt - 1;
+    int n = 0;
+    if (p.kind == K_SIMT_F32) {
+        n = snprintf(buf, len, "kernel=simt_f32_kernel launches=%d", P > 0 ? 2 : 1);
+    } else if (p.kind == K_TC_BF16_HEAD) {
+        HeadLaunch hl;
+        memset(&hl, 0, sizeof(hl));
+        if (!head_configure(T, p.H, p.W, p.Cin, p.Cout, 1, &hl)) return CC3D_ERR_UNSUPPORTED;
+        n = snprintf(buf, len,
+                     "kernel=head_bf16_kernel frames_per_pass=%d column_strips=%d row_stages=%d row_stage_bytes=%d "
+                     "weight_bytes=%d tmem_cols=%d smem_bytes=%zu units=%lld",
+                     hl.gmax, hl.ncolblk, hl.nstages, hl.x_stage_bytes, hl.w_bytes, hl.tmem_cols, hl.smem_bytes,
+                     hl.units);
+    } else if (p.kind == K_TC_BF16_STREAM) {
+        StreamLaunch sl;
+        memset(&sl, 0, sizeof(sl));
+        if (!stream_configure(T, p.H, p.W, p.Cin, p.Cout, p.kt, 1, &sl)) return CC3D_ERR_UNSUPPORTED;
+        n = snprintf(buf, len,
+                     "kernel=stream_bf16_kernel frames_per_unit=%d position_blocks=%d stages=%d stage_bytes=%d "
+                     "weight_bytes=%d tmem_cols=%d smem_bytes=%zu units=%lld",
+                     sl.gmax, sl.npb, sl.nstages, sl.x_stage_bytes, sl.w_bytes, sl.tmem_cols, sl.smem_bytes, sl.units);
+    } else {
+        TcLaunch L;
+        memset(&L, 0, sizeof(L));
+        if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, has_residual != 0, p.up2 != 0, &L))
+            return CC3D_ERR_UNSUPPORTED;
+        const int tiles = L.g.tiles_per_cb * L.g.ncolblk * (L.tstack ? (T + 1) / 2 : T) * L.ncoblk;
+        // history frames the forward call hands to a copy engine (when the side stream is available)
+        const int n_ce = P == 0 ? 0 : (L.pair && !L.tstack ? P : (L.tstack ? 1 : 0));
+        n = snprintf(buf, len,
+                     "kernel=%s pair=%d two_frame=%d up2=%d channel_block=%d NT=%d nsplit=%d cout_blocks=%d "
+                     "row_groups=%d column_block=%d row_aligned=%d window_rows=%d tap_rows_per_weight_stage=%d "
+                     "window_stages=%d weight_stages=%d window_stage_bytes=%d weight_stage_bytes=%d acc_stages=%d "
+                     "mma_warps=%d split_n=%d tmem_cols=%d smem_bytes=%zu tiles=%d history_frames_on_copy_engine=%d",
+                     L.tstack ? "tc2s_bf16_kernel" : (L.pair ? "tc2_bf16_kernel" : "tc_bf16_kernel"), L.pair,
+                     L.tstack, L.up2, p.CB, L.NT, L.nsplit, L.ncoblk, L.g.sub, L.g.S, L.g.row_aligned, L.g.nrows,
+                     L.rb, L.na, L.nb, L.a_stage_bytes, L.b_stage_bytes, L.acc_stages, L.issuers, L.split_n,
+                     L.tmem_cols, L.smem_bytes, tiles, n_ce);
+    }
+    if (n < 0 || (size_t)n >= len) {
+        buf[0] = 0;
+        return CC3D_ERR_INVALID_ARG;
+    }
+    return CC3D_OK;
 }
 
 cc3d_status cc3d_debug_set_wait_budget_ns(cc3d_plan_t plan, unsigned long long ns)

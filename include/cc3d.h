@@ -215,6 +215,22 @@ const char* cc3d_plan_kernel(cc3d_plan_t plan);
  * (T_chunk >= 1). */
 int cc3d_plan_launches_per_chunk(cc3d_plan_t plan);
 
+/* The launch configuration cc3d_forward_chunk would use for a chunk of T_chunk
+ * frames (with a residual when has_residual != 0), as one line of
+ * space-separated key=value pairs, NUL-terminated, written into buf (len bytes,
+ * owned by the caller).  Host-only: no device is needed and nothing is
+ * launched.  Keys for the tensor-core families: kernel (the CUDA kernel:
+ * tc_bf16_kernel on one SM, tc2_bf16_kernel on SM pairs, tc2s_bf16_kernel on
+ * SM pairs with two output frames per MMA), pair, two_frame, up2,
+ * channel_block, NT (output channels per tile), row_groups (128-row groups per
+ * tile), window_stages / weight_stages and their bytes, tap_rows_per_weight_stage,
+ * acc_stages, smem_bytes, tiles (per chunk) and history_frames_on_copy_engine;
+ * the head, streaming and fp32 families report their own keys.  Returns
+ * CC3D_ERR_INVALID_ARG for a NULL plan or buf, T_chunk < 1, or a line longer
+ * than len - 1 (buf is then the empty string); CC3D_ERR_UNSUPPORTED when the
+ * chunk has no configuration. */
+cc3d_status cc3d_plan_describe(cc3d_plan_t plan, int T_chunk, int has_residual, char* buf, size_t len);
+
 /*
  * Test hooks (used by the fault tests; never needed in normal use).
  * cc3d_debug_set_wait_budget_ns: wall-clock budget of every bounded wait in

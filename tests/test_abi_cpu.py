@@ -170,3 +170,85 @@ def test_every_supported_bf16_shape_gets_a_configuration(lib, C):
             cc3d.cc3d_destroy(p)
         p = cc3d.cc3d_plan_create_upsample2x(C, C, 32, 100, 3, cc3d.CC3D_BF16)
         cc3d.cc3d_destroy(p)
+
+
+# The launch configuration each decoder layer's chunk gets (host-only): the kernel, its stage
+# rings and its tile count, as measured and described in the design notes.  A change to the
+# selection logic shows up here before any GPU run.
+@pytest.mark.parametrize("plan_args,T,expect", [
+    (dict(Cin=96, Cout=96, H=360, W=640), 4,
+     dict(kernel="tc2s_bf16_kernel", pair=1, two_frame=1, NT=96, row_aligned=1, tap_rows_per_weight_stage=3,
+          window_stages=3, weight_stages=2, acc_stages=1, smem_bytes=213376, tiles=1800,
+          history_frames_on_copy_engine=1)),
+    (dict(Cin=96, Cout=96, H=360, W=640), 1,
+     dict(kernel="tc2_bf16_kernel", pair=1, two_frame=0, acc_stages=2, tiles=900, history_frames_on_copy_engine=2)),
+    (dict(Cin=192, Cout=192, H=180, W=320), 4,
+     dict(kernel="tc2_bf16_kernel", row_aligned=0, NT=192, tap_rows_per_weight_stage=1, weight_stages=6,
+          tiles=912, history_frames_on_copy_engine=2)),
+    (dict(Cin=192, Cout=192, H=180, W=320), 3,
+     dict(kernel="tc_bf16_kernel", pair=0, weight_stages=3, history_frames_on_copy_engine=0)),
+    (dict(Cin=384, Cout=384, H=90, W=160), 4, dict(kernel="tc2_bf16_kernel", cout_blocks=2, NT=192, tiles=456)),
+    (dict(Cin=384, Cout=192, H=90, W=160), 4, dict(kernel="tc2_bf16_kernel", cout_blocks=1, tiles=228)),
+    (dict(Cin=96, Cout=96, H=1440, W=2560), 4, dict(kernel="tc2s_bf16_kernel", tiles=28800)),
+    (dict(Cin=96, Cout=96, H=360, W=640, kt=2), 4,
+     dict(kernel="tc2s_bf16_kernel", two_frame=1, history_frames_on_copy_engine=1)),
+    (dict(Cin=96, Cout=3, H=1440, W=2560), 4, dict(kernel="head_bf16_kernel", column_strips=21)),
+    (dict(Cin=96, Cout=96, H=360, W=640, kt=3, kh=1, kw=1), 4,
+     dict(kernel="stream_bf16_kernel", position_blocks=1800)),
+    (dict(Cin=16, Cout=16, H=32, W=32, dtype="f32"), 4, dict(kernel="simt_f32_kernel", launches=2)),
+])
+def test_describe_reports_the_measured_configurations(lib, plan_args, T, expect):
+    plan = cc3d.CausalConv3dPlan(**plan_args)
+    try:
+        got = plan.describe(T)
+    finally:
+        plan.close()
+    assert {k: got.get(k) for k in expect} == expect
+
+
+def test_describe_of_the_fused_upsample_plan(lib):
+    plan = cc3d.Upsample2xConvPlan(96, 96, 180, 320)
+    try:
+        got = plan.describe(4)
+    finally:
+        plan.close()
+    assert got["kernel"] == "tc_bf16_kernel" and got["up2"] == 1 and got["pair"] == 0
+
+
+@pytest.mark.parametrize("C", [16, 32, 64, 96, 192, 384])
+def test_every_tensor_core_configuration_fits_the_sm(lib, C):
+    # shared memory within the 227 KB a block may take (static barriers included), tensor memory
+    # within 512 columns, at least double-buffered rings, and the two-frame schedule only where
+    # the epilogue can hold two 96-column row groups
+    for Cout in (C, C // 2 if C >= 32 else C):
+        for H, W in ((8, 100), (360, 640), (90, 160), (1440, 2560), (5, 254)):
+            for kt in (2, 3):
+                plan = cc3d.CausalConv3dPlan(C, Cout, H, W, kt)
+                try:
+                    for T in (1, 2, 3, 4, 5):
+                        d = plan.describe(T, has_residual=(T % 2 == 0))
+                        assert d["kernel"] in ("tc_bf16_kernel", "tc2_bf16_kernel", "tc2s_bf16_kernel")
+                        assert d["smem_bytes"] + 1024 <= 227 * 1024, d
+                        assert d["tmem_cols"] <= 512 and d["tmem_cols"] & (d["tmem_cols"] - 1) == 0, d
+                        assert 2 <= d["window_stages"] <= 8 and 2 <= d["weight_stages"] <= 8, d
+                        assert d["tiles"] >= 1
+                        if d["two_frame"]:
+                            assert d["pair"] == 1 and d["NT"] <= 96 and T >= 2, d
+                finally:
+                    plan.close()
+
+
+def test_describe_rejects_bad_arguments(lib):
+    plan = cc3d.cc3d_plan_create(96, 96, 360, 640, 3, 3, 3, cc3d.CC3D_BF16)
+    try:
+        buf = ctypes.create_string_buffer(16)
+        assert lib.cc3d_plan_describe(plan, 4, 1, buf, len(buf)) == 1  # line longer than the buffer
+        assert buf.value == b""
+        big = ctypes.create_string_buffer(1024)
+        assert lib.cc3d_plan_describe(plan, 0, 1, big, len(big)) == 1
+        assert lib.cc3d_plan_describe(None, 4, 1, big, len(big)) == 1
+        assert lib.cc3d_plan_describe(plan, 4, 1, None, 0) == 1
+        assert lib.cc3d_plan_describe(plan, 4, 1, big, len(big)) == 0
+        assert big.value.startswith(b"kernel=tc2s_bf16_kernel ")
+    finally:
+        cc3d.cc3d_destroy(plan)

@@ -324,12 +324,36 @@ class CausalConv3dPlan:
             self.reset(c)
         return c
 
+    def _check_sizes(self, T, y_dtype, **tensors):
+        """Element counts and dtypes of the tensor arguments against the plan.  The C ABI takes
+        bare pointers and cannot see a buffer's size, so a tensor of the wrong shape would be read
+        or written past its end; this catches it before the call (integer addresses and None are
+        passed through unchecked)."""
+        dt = self.torch_dtype()
+        hist = (self.kt - 1) * self.H * self.W * self.Cin
+        out = T * self.Ho * self.Wo * self.Cout
+        need = {"x": (T * self.H * self.W * self.Cin, dt),
+                "w": (self.Cout * self.kt * self.kh * self.kw * self.Cin, dt),
+                "b": (self.Cout, dt), "residual": (out, dt), "cache_in": (hist, dt), "cache_out": (hist, dt),
+                "cache": (hist, dt), "y": (out, y_dtype)}
+        for name, t in tensors.items():
+            if t is None or isinstance(t, int):
+                continue
+            n, d = need[name]
+            if t.dtype != d:
+                raise ValueError("%s has dtype %s; this plan takes %s" % (name, t.dtype, d))
+            if t.numel() != n:
+                raise ValueError("%s has %d elements (shape %s); this plan takes %d"
+                                 % (name, t.numel(), tuple(t.shape), n))
+
     def forward_chunk(self, x, w, b=None, residual=None, cache_in=None, cache_out=None, y=None, stream=None):
         """Enqueue one chunk; returns y ([T][H][W][Cout]).  cache_out receives the new history."""
         import torch
         T = 0 if x is None else int(x.shape[0])
         if y is None and T > 0:
             y = torch.empty((T, self.Ho, self.Wo, self.Cout), dtype=self.torch_dtype(), device=x.device)
+        self._check_sizes(T, self.torch_dtype(), x=x, w=w, b=b, residual=residual, cache_in=cache_in,
+                          cache_out=cache_out, y=y)
         cc3d_forward_chunk(self.handle, T, x, w, b, residual, cache_in, cache_out, y, stream)
         return y
 
@@ -339,10 +363,13 @@ class CausalConv3dPlan:
         T = 0 if x is None else int(x.shape[0])
         if y is None and T > 0:
             y = torch.empty((T, self.Ho, self.Wo, self.Cout), dtype=torch.uint8, device=x.device)
+        self._check_sizes(T, torch.uint8, x=x, w=w, b=b, residual=residual, cache_in=cache_in,
+                          cache_out=cache_out, y=y)
         cc3d_forward_chunk_u8(self.handle, T, x, w, b, residual, cache_in, cache_out, y, stream)
         return y
 
     def reset(self, cache, stream=None):
+        self._check_sizes(0, self.torch_dtype(), cache=cache)
         cc3d_reset(self.handle, cache, stream)
 
     def status(self, stream=None) -> int:

@@ -252,3 +252,48 @@ def test_describe_rejects_bad_arguments(lib):
         assert big.value.startswith(b"kernel=tc2s_bf16_kernel ")
     finally:
         cc3d.cc3d_destroy(plan)
+
+
+def test_plan_methods_check_tensor_sizes_before_the_call(lib):
+    # the C ABI sees bare pointers: the plan object rejects a tensor whose element count or dtype
+    # does not match the plan before any pointer reaches the library
+    import torch
+    bf = torch.bfloat16
+    T, H, W, C = 2, 4, 8, 32
+    plan = cc3d.CausalConv3dPlan(C, C, H, W)
+    x = torch.zeros((T, H, W, C), dtype=bf)
+    w = torch.zeros((C, 3, 3, 3, C), dtype=bf)
+    y = torch.zeros((T, H, W, C), dtype=bf)
+    cache = torch.zeros((2, H, W, C), dtype=bf)
+    bad = [
+        dict(x=torch.zeros((T, H, W, C // 2), dtype=bf)),
+        dict(w=torch.zeros((C, 2, 3, 3, C), dtype=bf)),
+        dict(b=torch.zeros((C + 1,), dtype=bf)),
+        dict(residual=torch.zeros((T + 1, H, W, C), dtype=bf)),
+        dict(cache_in=torch.zeros((1, H, W, C), dtype=bf)),
+        dict(cache_out=torch.zeros((2, H, W + 1, C), dtype=bf)),
+        dict(y=torch.zeros((T, H, W, C), dtype=torch.float32)),
+        dict(w=torch.zeros((C, 3, 3, 3, C), dtype=torch.float32)),
+    ]
+    for kw in bad:
+        args = dict(x=x, w=w, b=None, residual=None, cache_in=None, cache_out=cache, y=y)
+        args.update(kw)
+        with pytest.raises(ValueError, match=next(iter(kw))):
+            plan.forward_chunk(**args)
+    with pytest.raises(ValueError, match="cache"):
+        plan.reset(torch.zeros((3, H, W, C), dtype=bf))
+    with pytest.raises(ValueError, match="y has dtype"):
+        plan.forward_chunk_u8(x, w, None, None, None, cache, y)
+    # matching sizes pass the check and stop at the device-memory check of the binding
+    with pytest.raises(ValueError, match="CUDA"):
+        plan.forward_chunk(x, w, None, None, None, cache, y)
+    plan.close()
+    # the fused upsample: outputs and residual are 2H x 2W, the history holds source frames
+    up = cc3d.Upsample2xConvPlan(C, C, H, W)
+    with pytest.raises(ValueError, match="residual"):
+        up.forward_chunk(x, w, None, torch.zeros((T, H, W, C), dtype=bf), None, cache,
+                         torch.zeros((T, 2 * H, 2 * W, C), dtype=bf))
+    with pytest.raises(ValueError, match="CUDA"):
+        up.forward_chunk(x, w, None, torch.zeros((T, 2 * H, 2 * W, C), dtype=bf), None, cache,
+                         torch.zeros((T, 2 * H, 2 * W, C), dtype=bf))
+    up.close()

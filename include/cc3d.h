@@ -57,6 +57,8 @@
 #ifndef CC3D_H
 #define CC3D_H
 
+#include <stddef.h> /* size_t */
+
 #ifdef __cplusplus
 extern "C" {
 #endif

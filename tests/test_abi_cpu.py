@@ -297,3 +297,48 @@ def test_plan_methods_check_tensor_sizes_before_the_call(lib):
         up.forward_chunk(x, w, None, torch.zeros((T, 2 * H, 2 * W, C), dtype=bf), None, cache,
                          torch.zeros((T, 2 * H, 2 * W, C), dtype=bf))
     up.close()
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "cc3d.h"
+
+int main(void)
+{
+    cc3d_plan_t plan = NULL;
+    char line[1024];
+    cc3d_status s = cc3d_plan_create(96, 96, 360, 640, 3, 3, 3, CC3D_BF16, &plan);
+    if (s != CC3D_OK) { printf("create: %s\n", cc3d_status_string(s)); return 1; }
+    s = cc3d_plan_describe(plan, 4, 1, line, sizeof line);
+    if (s != CC3D_OK) { printf("describe: %s\n", cc3d_status_string(s)); return 2; }
+    printf("%s\n%s\n", cc3d_plan_kernel(plan), line);
+    /* argument checks run on the host before any device work */
+    s = cc3d_forward_chunk(plan, 4, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL);
+    printf("forward without buffers: %d\n", (int)s);
+    cc3d_destroy(plan);
+    cc3d_destroy(NULL);
+    return 0;
+}
+"""
+
+
+def test_a_plain_c_program_compiles_links_and_calls_the_library(lib, tmp_path):
+    # the boundary is a C ABI: the header compiles as strict C99 on its own, and a C program links
+    # libcc3d.so and calls its host-only entry points with no Python or PyTorch involved
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_cc3d.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_cc3d"
+    libdir = os.path.dirname(cc3d.library_path())
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.dirname(HEADER),
+                    str(src), "-o", str(exe), "-L", libdir, "-lcc3d", "-Wl,-rpath," + libdir],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True, timeout=120).stdout.splitlines()
+    assert out[0] == "tc_bf16_pair"
+    assert out[1].startswith("kernel=tc2s_bf16_kernel ")
+    assert out[2] == "forward without buffers: 1"

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(9):
+    for code in range(10):
         s = cc3d.cc3d_status_string(code)
         assert s and s != "unknown status"
     assert cc3d.cc3d_status_string(99) == "unknown status"

@@ -546,7 +546,9 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
     // ---- presence
     if (P > 0 && cache_out == nullptr) return CC3D_ERR_INVALID_ARG;
     if (T > 0 && (x == nullptr || w == nullptr || y == nullptr)) return CC3D_ERR_INVALID_ARG;
-    if ((long long)T * p.H * p.W > (1LL << 40)) return CC3D_ERR_UNSUPPORTED;
+    // every tile and unit index of the kernels stays within int (2^33 positions of even 16 bf16
+    // channels are 275 GB, more than the device holds)
+    if ((long long)T * p.H * p.W > (1LL << 33)) return CC3D_ERR_UNSUPPORTED;
     // ---- alignment.  fp32: one element.  bf16: 16 bytes for everything the tensor-core kernel
     // moves with TMA or 16-byte vectors (x, w, caches, and y / residual when Cout is a multiple
     // of 16); the narrow head stores y and reads the residual and bias per element.

@@ -123,7 +123,8 @@ cc3d_status cc3d_plan_create_upsample2x(int Cin, int Cout, int H, int W, int kt,
  *            cache_in, x_chunk, y or residual (ping-pong two buffers).
  *   y        [T_chunk][H][W][Cout] output; must not overlap any input.
  * T_chunk may be 0: then only cache_out is written (it receives cache_in, or
- * zeros), and x_chunk, residual and y may be NULL.
+ * zeros), and x_chunk, residual and y may be NULL.  A chunk of more than 2^33
+ * positions (T_chunk * H * W) returns CC3D_ERR_UNSUPPORTED.
  * The result of every output element does not depend on how the video is
  * split into chunks (bit-identical across chunkings).
  * Returns CC3D_OK once the work is enqueued; asynchronous failures surface in

@@ -106,6 +106,7 @@ def test_forward_rejects_before_any_device_work(lib):
         assert f(p, -1, x, w, None, None, None, c1, y, None) == 1            # negative T
         assert f(p, 1, None, w, None, None, None, c1, y, None) == 1          # missing x
         assert f(p, 1, x, w, None, None, None, None, y, None) == 1           # missing cache_out
+        assert f(p, 1 << 29, x, w, None, None, None, c1, y, None) == 2       # 2^34 positions in one chunk
         assert f(p, 1, x + 8, w, None, None, None, c1, y, None) == 3         # misaligned
         assert f(p, 1, x, w, None, None, None, c1, x, None) == 4             # y overlaps x
         assert f(p, 1, x, w, None, None, c0, c0, y, None) == 4               # cache_out overlaps cache_in

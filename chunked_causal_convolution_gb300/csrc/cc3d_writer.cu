@@ -194,6 +194,8 @@ cc3d_status cc3d_writer_close(cc3d_writer_t w, long long* bytes_written)
     int st = w->error;
     if (bytes_written) *bytes_written = w->bytes_written;
     if (fflush(w->file) != 0 && st == CC3D_OK) st = CC3D_ERR_IO;
+    if (fclose(w->file) != 0 && st == CC3D_OK) st = CC3D_ERR_IO;
+    w->file = nullptr;
     writer_free(w);
     return (cc3d_status)st;
 }

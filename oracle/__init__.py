@@ -212,3 +212,40 @@ def upsample_nearest2x(x):
 def conv_upsample2x_whole(x, w, b=None, r=None, nthreads=None, _lib=None):
     """The convolution of the nearest-2x upsampled sequence: conv_whole(upsample_nearest2x(x))."""
     return conv_whole(upsample_nearest2x(x), w, b, r, nthreads=nthreads, _lib=_lib)
+
+
+def round_bf16(y):
+    """Round float64 values to the nearest bfloat16 value, ties to even, returned as float64.
+
+    bfloat16 keeps 8 significant bits and float32's 8-bit exponent.  For y = m * 2**e with
+    0.5 <= |m| < 1 the representable neighbours of y are spaced 2**(e - 8) apart (the spacing stays
+    2**-133 below the normal range, e < -125); y is scaled by that spacing, rounded half to even and
+    scaled back, which is exact in float64.  Magnitudes that round to 2**128 or beyond become inf;
+    NaN stays NaN.  (The outputs of the decoder's convolution are stored as bfloat16: "SwiftVR
+    Inference Optimization" (LightX2V blog) runs the VAE in BF16.)"""
+    y = _f64(y)
+    with np.errstate(invalid="ignore"):
+        _, e = np.frexp(y)
+        step = np.maximum(e, -125) - 8
+        r = np.ldexp(np.rint(np.ldexp(y, -step)), step)
+        return np.where(np.abs(r) >= 2.0 ** 128, np.copysign(np.inf, y), r)
+
+
+def quantize_u8(y):
+    """8-bit pixels of the decoder's output frames (the device-side half of the asynchronous frame
+    output path: "How Synthesia optimizes generative AI video inference on Amazon EC2 G7e
+    instances" copies finished frames to the host while the next chunk computes, and 8-bit frames
+    halve those copies).  The pages name 8-bit frames but not the mapping; the reading taken is the
+    plain one for decoder outputs in [-1, 1]:
+
+        v = round_bf16(y)                            (the value the bf16 output stores)
+        t = fp32(fp32(v + 1) * 127.5)                 (float32, one rounding per operation)
+        q = clamp(round_half_even(t), 0, 255)
+
+    y: float64 array of exact convolution outputs.  Returns uint8 of the same shape.  NaN inputs
+    have no defined pixel."""
+    v = round_bf16(y).astype(np.float32)  # exact: every bfloat16 value is a float32 value
+    t = (v + np.float32(1.0)).astype(np.float32)
+    t = (t * np.float32(127.5)).astype(np.float32)
+    with np.errstate(invalid="ignore"):
+        return np.clip(np.rint(t), 0.0, 255.0).astype(np.uint8)

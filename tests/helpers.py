@@ -65,3 +65,4 @@ def run_chunks(plan, x, w, b, r, chunks, stream=None, zero_cache_first=False):
 
 def compositions_sample():
     return [[24], [4] * 6, [1, 23], [5, 5, 5, 5, 4], [3, 1, 4, 1, 5, 10]]
+

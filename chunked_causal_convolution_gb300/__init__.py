@@ -28,7 +28,8 @@ __all__ = [
     "cc3d_plan_create", "cc3d_plan_create_upsample2x", "cc3d_forward_chunk", "cc3d_forward_chunk_u8",
     "cc3d_reset", "cc3d_get_status", "cc3d_destroy", "cc3d_status_string", "cc3d_plan_kernel",
     "cc3d_plan_launches_per_chunk", "cc3d_plan_describe", "cc3d_debug_set_wait_budget_ns",
-    "cc3d_debug_set_fault", "cc3d_last_error_detail", "library_path", "Upsample2xConvPlan",
+    "cc3d_debug_set_fault", "cc3d_debug_set_schedule", "SCHEDULE_KNOBS", "cc3d_last_error_detail",
+    "library_path", "Upsample2xConvPlan",
     "load_library", "FrameWriter",
     "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
     "weights_from_torch_layout", "EXPORTED_SYMBOLS",
@@ -47,9 +48,15 @@ EXPORTED_SYMBOLS = (
     "cc3d_plan_create", "cc3d_plan_create_upsample2x", "cc3d_forward_chunk", "cc3d_forward_chunk_u8", "cc3d_reset", "cc3d_get_status",
     "cc3d_destroy",
     "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk", "cc3d_plan_describe",
-    "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_last_error_detail",
+    "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_debug_set_schedule", "cc3d_last_error_detail",
     "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
 )
+
+# the CC3D_SCHED_* knobs of cc3d.h, by name (value -1 restores the measured default)
+SCHEDULE_KNOBS = {
+    "pair": 0, "two_frame": 1, "split_tail": 2, "channel_blocks": 3, "mma_warps": 4, "row_groups": 5,
+    "acc_stages": 6, "tap_rows": 7, "window_stages": 8, "weight_stages": 9, "prefetch": 10,
+}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -98,6 +105,7 @@ def load_library():
         lib.cc3d_plan_describe.argtypes = [vp, i, i, ctypes.c_char_p, ctypes.c_size_t]
         lib.cc3d_debug_set_wait_budget_ns.argtypes = [vp, u64]
         lib.cc3d_debug_set_fault.argtypes = [vp, i]
+        lib.cc3d_debug_set_schedule.argtypes = [vp, i, i]
         lib.cc3d_writer_create.argtypes = [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(vp)]
         lib.cc3d_writer_submit.argtypes = [vp, vp, ctypes.c_size_t, vp, ctypes.POINTER(ctypes.c_longlong)]
         lib.cc3d_writer_wait_copied.argtypes = [vp, ctypes.c_longlong, vp]
@@ -110,7 +118,7 @@ def load_library():
         for f in (lib.cc3d_plan_create, lib.cc3d_plan_create_upsample2x, lib.cc3d_forward_chunk, lib.cc3d_forward_chunk_u8, lib.cc3d_reset,
                   lib.cc3d_get_status,
                   lib.cc3d_plan_launches_per_chunk, lib.cc3d_plan_describe, lib.cc3d_debug_set_wait_budget_ns,
-                  lib.cc3d_debug_set_fault):
+                  lib.cc3d_debug_set_fault, lib.cc3d_debug_set_schedule):
             f.restype = i
         _lib = lib
         return lib
@@ -147,9 +155,19 @@ def _addr(t):
         return t or None
     if not t.is_cuda:
         raise ValueError("tensor arguments must be CUDA tensors")
+    _check_device(t)
     if not t.is_contiguous():
         raise ValueError("tensor arguments must be contiguous")
     return t.data_ptr() or None
+
+
+def _check_device(t):
+    """The library launches on the current device; a tensor of another device would be read
+    through that device's addresses, so it is refused here (the C ABI refuses it too)."""
+    import torch
+    cur = torch.cuda.current_device()
+    if t.device.index is not None and t.device.index != cur:
+        raise ValueError("tensor on %s, but the current device is cuda:%d" % (t.device, cur))
 
 
 def _stream(stream):
@@ -284,6 +302,13 @@ def cc3d_debug_set_fault(plan, mode: int):
     _check(load_library().cc3d_debug_set_fault(plan, int(mode)), "cc3d_debug_set_fault")
 
 
+def cc3d_debug_set_schedule(plan, knob, value: int):
+    """Override one schedule knob of the plan (a CC3D_SCHED_* number or a SCHEDULE_KNOBS name);
+    -1 restores the measured default."""
+    k = SCHEDULE_KNOBS[knob] if isinstance(knob, str) else int(knob)
+    _check(load_library().cc3d_debug_set_schedule(plan, k, int(value)), "cc3d_debug_set_schedule")
+
+
 # ---------------------------------------------------------------- convenience
 def weights_from_torch_layout(w_oikkk):
     """PyTorch Conv3d weights [Cout][Cin][kt][kh][kw] -> this library's [Cout][kt][kh][kw][Cin]."""
@@ -380,6 +405,10 @@ class CausalConv3dPlan:
 
     def set_fault(self, mode):
         cc3d_debug_set_fault(self.handle, mode)
+
+    def set_schedule(self, knob, value):
+        """Override one schedule knob (name from SCHEDULE_KNOBS); -1 restores the default."""
+        cc3d_debug_set_schedule(self.handle, knob, value)
 
     def close(self):
         if getattr(self, "handle", None):

@@ -16,8 +16,20 @@
 
 namespace cc3d {
 
-// Per-device status word: kernels or-in STATUS_* bits, cc3d_get_status reads and clears it.
+// Per-device status word: kernels or-in STATUS_* bits, cc3d_get_status reads and clears it.  It is
+// shared by every plan on the device: a timeout of one plan is reported to whichever caller of
+// cc3d_get_status on that device comes first.
 __device__ unsigned g_status_word;
+// cc3d_get_status's read of the word, taken and cleared in one atomic exchange
+__device__ unsigned g_status_taken;
+
+__global__ void status_take_kernel() { g_status_taken = atomicExch(&g_status_word, 0u); }
+
+cudaError_t status_take_launch(cudaStream_t stream)
+{
+    status_take_kernel<<<1, 1, 0, stream>>>();
+    return cudaGetLastError();
+}
 
 namespace {
 
@@ -41,6 +53,7 @@ struct DeviceInfo {
 };
 
 std::mutex g_mutex;
+std::mutex g_status_mutex;
 thread_local const char* g_last_detail = "none";
 
 // Record what failed (for cc3d_last_error_detail) and return CC3D_ERR_CUDA.
@@ -86,14 +99,25 @@ cc3d_status device_info(DeviceInfo** out)
     return CC3D_OK;
 }
 
-bool is_device_ptr(const void* p)
+// Where a tensor pointer lives: CC3D_OK for memory the current device's kernels may use (its own
+// device memory, or managed memory), CC3D_ERR_NOT_DEVICE_MEMORY for host or unknown memory, and
+// CC3D_ERR_INVALID_ARG for another device's memory (the kernels, tensor maps and status word are
+// those of the current device, and without peer access such a read faults).
+cc3d_status pointer_check(const void* p)
 {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
         cudaGetLastError();  // clear the non-sticky error
-        return false;
+        return CC3D_ERR_NOT_DEVICE_MEMORY;
     }
-    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+    if (a.type == cudaMemoryTypeManaged) return CC3D_OK;
+    if (a.type != cudaMemoryTypeDevice) return CC3D_ERR_NOT_DEVICE_MEMORY;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return CC3D_ERR_NOT_DEVICE_MEMORY;
+    }
+    return a.device == dev ? CC3D_OK : CC3D_ERR_INVALID_ARG;
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb)
@@ -118,6 +142,7 @@ struct cc3d_plan_s {
     int CB;
     unsigned long long wait_ns;
     int fault;
+    TcOverrides ov;  // schedule knobs (cc3d_debug_set_schedule), all -1 = measured defaults
     // Part of the new history is copied by a copy engine on a side stream, forked from the
     // caller's stream before the launch and joined to it after (created on first use, on the
     // device current then; on another device the kernel copies the whole history itself): all of
@@ -338,8 +363,8 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
         } else {
             TcLaunch probe;
             memset(&probe, 0, sizeof(probe));
-            if (!tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, false, false, &probe) ||
-                !tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, true, false, &probe))
+            if (!tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, false, false, nullptr, &probe) ||
+                !tc_configure(CB, 1, H, W, Cin, Cout, kt, kh, true, false, nullptr, &probe))
                 return CC3D_ERR_UNSUPPORTED;
             kind = Cout < 16 ? K_TC_BF16_NARROW : (probe.pair ? K_TC_BF16_PAIR : K_TC_BF16);
         }
@@ -358,6 +383,7 @@ cc3d_status cc3d_plan_create(int Cin, int Cout, int H, int W, int kt, int kh, in
     p->CB = CB;
     p->wait_ns = 2000000000ull;
     p->fault = 0;
+    for (int& v : p->ov.v) v = -1;
     *out = p;
     return CC3D_OK;
 }
@@ -375,8 +401,8 @@ cc3d_status cc3d_plan_create_upsample2x(int Cin, int Cout, int H, int W, int kt,
     const int CB = (Cin % 32 == 0) ? 32 : 16;
     TcLaunch probe;
     memset(&probe, 0, sizeof(probe));
-    if (!tc_configure(CB, 1, H, W, Cin, Cout, kt, 3, false, true, &probe) ||
-        !tc_configure(CB, 1, H, W, Cin, Cout, kt, 3, true, true, &probe))
+    if (!tc_configure(CB, 1, H, W, Cin, Cout, kt, 3, false, true, nullptr, &probe) ||
+        !tc_configure(CB, 1, H, W, Cin, Cout, kt, 3, true, true, nullptr, &probe))
         return CC3D_ERR_UNSUPPORTED;
     cc3d_plan_s* p = new (std::nothrow) cc3d_plan_s;
     if (p == nullptr) return CC3D_ERR_OOM;
@@ -393,6 +419,7 @@ cc3d_status cc3d_plan_create_upsample2x(int Cin, int Cout, int H, int W, int kt,
     p->CB = CB;
     p->wait_ns = 2000000000ull;
     p->fault = 0;
+    for (int& v : p->ov.v) v = -1;
     *out = p;
     return CC3D_OK;
 }
@@ -450,7 +477,7 @@ cc3d_status cc3d_plan_describe(cc3d_plan_t plan, int T, int has_residual, char* 
     } else {
         TcLaunch L;
         memset(&L, 0, sizeof(L));
-        if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, has_residual != 0, p.up2 != 0, &L))
+        if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, has_residual != 0, p.up2 != 0, &p.ov, &L))
             return CC3D_ERR_UNSUPPORTED;
         const int tiles = L.g.tiles_per_cb * L.g.ncolblk * (L.tstack ? (T + 1) / 2 : T) * L.ncoblk;
         // history frames the forward call hands to a copy engine (when the side stream is available)
@@ -486,13 +513,30 @@ cc3d_status cc3d_debug_set_fault(cc3d_plan_t plan, int mode)
     return CC3D_OK;
 }
 
+cc3d_status cc3d_debug_set_schedule(cc3d_plan_t plan, int knob, int value)
+{
+    // [lo, hi] of every knob; value -1 restores the measured default
+    static const int range[CC3D_SCHED_COUNT][2] = {
+        {0, 1}, {0, 1}, {0, 1}, {0, 1}, {1, 2}, {1, 4}, {1, kMaxAccStages}, {1, 3}, {2, kMaxRingStages},
+        {2, kMaxRingStages}, {0, 3}};
+    if (plan == nullptr || knob < 0 || knob >= CC3D_SCHED_COUNT) return CC3D_ERR_INVALID_ARG;
+    if (value != -1) {
+        if (value < range[knob][0] || value > range[knob][1]) return CC3D_ERR_INVALID_ARG;
+        if (knob == CC3D_SCHED_ROW_GROUPS && value == 3) return CC3D_ERR_INVALID_ARG;
+        if (knob == CC3D_SCHED_TAP_ROWS && value == 2) return CC3D_ERR_INVALID_ARG;
+    }
+    plan->ov.v[knob] = value;
+    return CC3D_OK;
+}
+
 static size_t esize(const cc3d_plan_s* p) { return p->dtype == CC3D_F32 ? 4 : 2; }
 
 cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream)
 {
     if (plan == nullptr || cache == nullptr) return CC3D_ERR_INVALID_ARG;
     if (!aligned_to(cache, plan->dtype == CC3D_F32 ? 4 : 16)) return CC3D_ERR_ALIGNMENT;
-    if (!is_device_ptr(cache)) return CC3D_ERR_NOT_DEVICE_MEMORY;
+    const cc3d_status where = pointer_check(cache);
+    if (where != CC3D_OK) return where;
     const size_t bytes = (size_t)(plan->kt - 1) * plan->H * plan->W * plan->Cin * esize(plan);
     if (bytes == 0) return CC3D_OK;
     DeviceInfo* d = nullptr;
@@ -509,18 +553,22 @@ cc3d_status cc3d_get_status(cc3d_plan_t plan, void* stream)
     DeviceInfo* d = nullptr;
     cc3d_status st = device_info(&d);
     if (st != CC3D_OK) return st;
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    // one atomic exchange on the device reads and clears the word, so a bit that a kernel still
+    // running elsewhere ors in is either in this read or left for the next one; the snapshot word
+    // is shared, so the exchange and its read-back are serialised across host threads
     unsigned word = 0;
-    e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word));
-    if (e != cudaSuccess) return cuda_fail("read status word", e);
-    if (word != 0) {
-        const unsigned zero = 0;
-        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
-        if (e != cudaSuccess) return cuda_fail("clear status word", e);
-        return CC3D_ERR_DEVICE_TIMEOUT;
+    {
+        std::lock_guard<std::mutex> lock(g_status_mutex);
+        e = status_take_launch(s);
+        if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&word, g_status_taken, sizeof(word), 0,
+                                                            cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     }
-    return CC3D_OK;
+    if (e != cudaSuccess) return cuda_fail("read and clear the status word", e);
+    return word != 0 ? CC3D_ERR_DEVICE_TIMEOUT : CC3D_OK;
 }
 
 }  // extern "C"
@@ -579,9 +627,12 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
         if (P > 0 && overlaps(cache_out, n_cache, s.p, s.n)) return CC3D_ERR_ALIAS;
     }
     if (T > 0 && P > 0 && overlaps(y, n_y, cache_out, n_cache)) return CC3D_ERR_ALIAS;
-    // ---- device memory
-    for (const void* q : all)
-        if (q != nullptr && !is_device_ptr(q)) return CC3D_ERR_NOT_DEVICE_MEMORY;
+    // ---- device memory, of the current device
+    for (const void* q : all) {
+        if (q == nullptr) continue;
+        const cc3d_status where = pointer_check(q);
+        if (where != CC3D_OK) return where;
+    }
     DeviceInfo* d = nullptr;
     cc3d_status st = device_info(&d);
     if (st != CC3D_OK) return st;
@@ -624,7 +675,7 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
     // ---- tensor-core path
     TcLaunch L;
     memset(&L, 0, sizeof(L));
-    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, res != nullptr, p.up2 != 0, &L))
+    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, res != nullptr, p.up2 != 0, &p.ov, &L))
         return CC3D_ERR_UNSUPPORTED;
     if (p.fault == 2) return cuda_fail("injected tensor-map encode failure");  // nothing launched
     const CUtensorMapSwizzle sw = p.CB == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -691,8 +742,7 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
         // accumulator buffer: split those tiles into one-row-group units, each computed by both
         // MMA warps on half of the output channels, so every block gets about the same work
         // (c384 -> 192 at 90 x 160: 228 tiles = 152 whole + 76 split over 152 SMs).
-        const char* env = getenv("CC3D_TC_SPLIT");
-        const bool allow = env == nullptr || *env == 0 || atoi(env) != 0;
+        const bool allow = p.ov.get(CC3D_SCHED_SPLIT_TAIL, 1) != 0;
         const int R = ntiles % d->sms;
         if (allow && L.acc_stages == 1 && L.issuers == 2 && !L.split_n && !L.up2 && L.nsplit == 1 &&
             L.g.sub == 2 && L.NT % 32 == 0 && R > 0 && 2 * R <= d->sms) {

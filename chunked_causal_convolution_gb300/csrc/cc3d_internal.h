@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "cc3d.h"
+
 namespace cc3d {
 
 // Device status word bits (or-ed by kernels, read and cleared by cc3d_get_status).
@@ -82,10 +84,19 @@ struct TcLaunch {
     size_t smem_bytes;
 };
 
+// Schedule overrides of one plan (cc3d_debug_set_schedule): one value per CC3D_SCHED_* knob of
+// cc3d.h, -1 = the measured default.  They change how the work is tiled, never the result.
+constexpr int kMaxRingStages = 8;  // deepest window / weight ring of the tensor-core kernels
+constexpr int kMaxAccStages = 2;   // accumulator buffers in tensor memory
+struct TcOverrides {
+    int v[CC3D_SCHED_COUNT];
+    int get(int knob, int dflt) const { return v[knob] >= 0 ? v[knob] : dflt; }
+};
+
 // Pick tiles / pipeline depths for a tensor-core launch.  Returns false if the
-// shape has no configuration.
+// shape has no configuration.  ov may be null (every knob at its default).
 bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, bool up2,
-                  TcLaunch* L);
+                  const TcOverrides* ov, TcLaunch* L);
 cudaError_t tc_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 cudaError_t tc2_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 cudaError_t tc2s_launch(int CB, const TcLaunch& L, cudaStream_t stream);

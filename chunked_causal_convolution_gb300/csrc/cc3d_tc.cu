@@ -502,11 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bf16_kernel(const __grid_const
 
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-int env_int(const char* name, int dflt)
-{
-    const char* s = getenv(name);
-    return (s != nullptr && *s) ? atoi(s) : dflt;
-}
 
 template <int CB, int RB>
 void* kernel_for(int sub)
@@ -526,9 +521,10 @@ namespace {
 
 // One attempt at a configuration with at most sub_cap row groups per tile.
 bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, bool up2,
-                         int sub_cap, int smax, TcLaunch* L)
+                         int sub_cap, int smax, const TcOverrides* O, TcLaunch* L)
 {
     (void)has_residual;  // the measured best configuration does not depend on it today
+    auto ov = [O](int knob, int dflt) { return O != nullptr ? O->get(knob, dflt) : dflt; };
     if (CB != 16 && CB != 32) return false;
     if (Cin % CB != 0) return false;
     if (kt < 1 || kt > 3 || (ks != 1 && ks != 3)) return false;
@@ -566,7 +562,7 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
         if (ns > 4) return false;
         L->nsplit = ns;
         L->NT = Cout / ns;
-        if (ns > 1 && env_int("CC3D_TC_COBLK", 1)) {
+        if (ns > 1 && ov(CC3D_SCHED_CHANNEL_BLOCKS, 1)) {
             L->ncoblk = ns;
             L->nsplit = 1;
         }
@@ -597,8 +593,8 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
         sub = ntot <= 128 ? 4 : (ntot <= 256 ? 2 : 1);
         acc = 1;
     }
-    sub = env_int("CC3D_TC_SUB", sub);
-    acc = env_int("CC3D_TC_ACC", acc);
+    sub = ov(CC3D_SCHED_ROW_GROUPS, sub);
+    acc = ov(CC3D_SCHED_ACC_STAGES, acc);
     if (sub > sub_cap) sub = sub_cap;
     // SM pairs (cta_group::2): both tiles of a pair must use the same window offsets (row-aligned
     // geometry) and the same weights (one output-channel block); then each block holds half of
@@ -610,10 +606,10 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
     // (W a multiple of 128, equal offsets everywhere) still pairs a single channel block.
     L->pair = 0;
     const bool pair_tiles_match = T % 2 == 0 || (W % 128 == 0 && L->ncoblk == 1);
-    if (!up2 && pair_tiles_match && L->nsplit == 1 && L->NT >= 32 && L->NT <= 192 && env_int("CC3D_TC_PAIR", 1)) {
+    if (!up2 && pair_tiles_match && L->nsplit == 1 && L->NT >= 32 && L->NT <= 192 && ov(CC3D_SCHED_PAIR, 1)) {
         L->pair = 1;
-        sub = env_int("CC3D_TC_SUB", 2);
-        acc = env_int("CC3D_TC_ACC", 2 * 2 * L->NT <= 512 ? 2 : 1);
+        sub = ov(CC3D_SCHED_ROW_GROUPS, 2);
+        acc = ov(CC3D_SCHED_ACC_STAGES, 2 * 2 * L->NT <= 512 ? 2 : 1);
     }
     // two output frames per pair tile, stacked into N where an input frame is a tap of both
     // (chunks of two or more frames of a kt x 3 x 3 kernel with kt >= 2, up to 96 output channels;
@@ -621,7 +617,7 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
     // block, one accumulator buffer of 2 frames x 2 row groups x NT columns
     L->tstack = 0;
     if (L->pair && W % 128 == 0 && L->ncoblk == 1 && kt >= 2 && ks == 3 && T >= 2 && L->NT <= 96 && sub_cap >= 2 &&
-        env_int("CC3D_TC_TSTACK", 1)) {
+        ov(CC3D_SCHED_TWO_FRAME, 1)) {
         L->tstack = 1;
         sub = 2;
         acc = 1;
@@ -634,7 +630,7 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
     L->split_n = 0;
     if (up2) {
         L->issuers = 2;  // each MMA warp owns two of the four output classes
-    } else if (env_int("CC3D_TC_ISSUERS", 2) == 2) {
+    } else if (ov(CC3D_SCHED_MMA_WARPS, 2) == 2) {
         if (sub >= 2) {
             L->issuers = 2;
         } else if (L->nsplit == 2) {
@@ -681,31 +677,31 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
     // stage amortises the per-stage work of the MMA warps for narrow N with four row groups
     // (measured faster there; with two row groups the deeper 3-tap ring wins)
     L->rb = (ks == 3 && 9 * L->NT * rowb <= 64 * 1024 && (sub >= 4 || up2)) ? 3 : 1;
-    L->rb = env_int("CC3D_TC_RB", L->rb);
+    L->rb = ov(CC3D_SCHED_TAP_ROWS, L->rb);
     if (L->rb != 1 && L->rb != 3) return false;
     // weight rows of one block (the two-frame schedule's stacked stages hold a whole tap)
     const int b_rows = L->pair && !L->tstack ? L->NT / 2 : L->NT;
     // pairs: 9-tap weight stages in the row-aligned geometry (c96), 3-tap ones in the flat
     // geometry, whose wide windows leave room for only two 9-tap stages (the weight ring was the
     // wait there: c384 1960 against 1837 TFLOP/s)
-    if (L->pair) L->rb = env_int("CC3D_TC_RB", ks == 3 && W % 128 == 0 ? 3 : 1);
-    if (L->tstack) L->rb = env_int("CC3D_TC_RB", 3);  // 9-tap stages: measured 8 % faster than 3-tap on c96
+    if (L->pair) L->rb = ov(CC3D_SCHED_TAP_ROWS, ks == 3 && W % 128 == 0 ? 3 : 1);
+    if (L->tstack) L->rb = ov(CC3D_SCHED_TAP_ROWS, 3);  // 9-tap stages: measured 8 % faster than 3-tap on c96
     if ((L->rb != 1 && L->rb != 3) || ks % L->rb != 0) return false;
     L->b_stage_bytes = (ks * L->rb * b_rows * rowb + 1023) & ~1023;
     const int budget = 220 * 1024 - 4 * ntot * L->ncoblk;
     L->na = (L->a_stage_bytes > 40 * 1024) ? 2 : 3;
-    L->na = env_int("CC3D_TC_NA", L->na);
+    L->na = ov(CC3D_SCHED_WINDOW_STAGES, L->na);
     if (L->na < 2 || L->na > kMaxStages) return false;
     int nb = (budget - L->na * L->a_stage_bytes) / L->b_stage_bytes;
     if (nb > kMaxStages) nb = kMaxStages;
-    const int nb_env = env_int("CC3D_TC_NB", 0);
+    const int nb_env = ov(CC3D_SCHED_WEIGHT_STAGES, 0);
     if (nb_env >= 2 && nb_env < nb) nb = nb_env;
     if (nb < 2) {
         L->na = 2;
         nb = (budget - L->na * L->a_stage_bytes) / L->b_stage_bytes;
         if (nb > kMaxStages) nb = kMaxStages;
     }
-    if (nb < 2 && L->rb == 3 && env_int("CC3D_TC_RB", 0) == 0) {
+    if (nb < 2 && L->rb == 3 && ov(CC3D_SCHED_TAP_ROWS, 0) == 0) {
         // the 9-tap weight stages do not fit beside two windows: 3-tap stages
         L->rb = 1;
         L->b_stage_bytes = (ks * b_rows * rowb + 1023) & ~1023;
@@ -716,7 +712,7 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
     L->nb = nb;
     // L2 prefetch of the next tile's windows: 0 none, 1..3 = that many temporal taps (newest first);
     // off by default: measured slower on every decoder shape (it competes with the live working set)
-    L->prefetch = env_int("CC3D_TC_PREFETCH", 0);
+    L->prefetch = ov(CC3D_SCHED_PREFETCH, 0);
     if (L->prefetch < 0 || L->prefetch > 3) L->prefetch = 0;
     L->smem_bytes =
         (size_t)L->na * L->a_stage_bytes + (size_t)L->nb * L->b_stage_bytes + 4 * ntot * L->ncoblk + 1024;
@@ -728,14 +724,14 @@ bool tc_configure_capped(int CB, int T, int H, int W, int Cin, int Cout, int kt,
 }  // namespace
 
 bool tc_configure(int CB, int T, int H, int W, int Cin, int Cout, int kt, int ks, bool has_residual, bool up2,
-                  TcLaunch* L)
+                  const TcOverrides* ov, TcLaunch* L)
 {
     // the preferred tile height and column blocks of up to 254 pixels first; wide flat windows may
     // need fewer row groups, then narrower column blocks, to leave room for two windows and two
     // weight stages in shared memory
     for (int smax : {254, 128})
         for (int cap = 4; cap >= 1; cap /= 2)
-            if (tc_configure_capped(CB, T, H, W, Cin, Cout, kt, ks, has_residual, up2, cap, smax, L)) return true;
+            if (tc_configure_capped(CB, T, H, W, Cin, Cout, kt, ks, has_residual, up2, cap, smax, ov, L)) return true;
     return false;
 }
 

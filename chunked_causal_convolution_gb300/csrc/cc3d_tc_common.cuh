@@ -11,8 +11,8 @@ namespace tcc {
 using namespace ptx;
 
 constexpr int kThreads = 256;
-constexpr int kMaxStages = 8;
-constexpr int kMaxAcc = 2;
+constexpr int kMaxStages = kMaxRingStages;
+constexpr int kMaxAcc = kMaxAccStages;
 // sleep between polls of waits that usually last long (the epilogue waits for a whole tile), so
 // that those warps leave issue slots to the MMA warps sharing their schedulers; the loader polls
 // without sleeping (a late refill costs more than the issue slots)

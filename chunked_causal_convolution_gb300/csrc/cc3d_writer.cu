@@ -38,6 +38,7 @@ struct Job {
 struct cc3d_writer_s {
     FILE* file = nullptr;
     size_t slot_bytes = 0;
+    int device = -1;  // the device current at creation: its copy stream, and where src must live
     void* host[kSlots] = {nullptr, nullptr};
     cudaStream_t copy = nullptr;
     cudaEvent_t ready[kSlots] = {nullptr, nullptr};   // compute reached the submission
@@ -65,12 +66,20 @@ struct cc3d_writer_s {
                 queue.pop_front();
             }
             int err = CC3D_OK;
+            bool failed_before;
+            {
+                std::lock_guard<std::mutex> lock(mu);
+                failed_before = error != CC3D_OK;
+            }
+            // once a copy or a write has failed, the jobs queued behind it are dropped, not
+            // written: the file ends at the last chunk that reached it whole, never with a gap
+            // followed by later chunks
             if (cudaEventSynchronize(copied[j.slot]) != cudaSuccess) err = CC3D_ERR_CUDA;
-            else if (j.bytes && fwrite(host[j.slot], 1, j.bytes, file) != j.bytes) err = CC3D_ERR_IO;
+            else if (!failed_before && j.bytes && fwrite(host[j.slot], 1, j.bytes, file) != j.bytes) err = CC3D_ERR_IO;
             {
                 std::lock_guard<std::mutex> lock(mu);
                 if (err != CC3D_OK && error == CC3D_OK) error = err;
-                if (err == CC3D_OK) bytes_written += (long long)j.bytes;
+                if (err == CC3D_OK && !failed_before) bytes_written += (long long)j.bytes;
                 busy[j.slot] = false;
             }
             cv.notify_all();
@@ -106,6 +115,14 @@ cc3d_status cc3d_writer_create(const char* path, size_t slot_bytes, cc3d_writer_
         writer_free(w);
         return CC3D_ERR_IO;
     }
+    // whole slots are written at once: no stdio buffer, so a failed write leaves no part of a
+    // chunk behind to be flushed later
+    setvbuf(w->file, nullptr, _IONBF, 0);
+    if (cudaGetDevice(&w->device) != cudaSuccess) {
+        cudaGetLastError();
+        writer_free(w);
+        return CC3D_ERR_CUDA;
+    }
     bool ok = cudaStreamCreateWithFlags(&w->copy, cudaStreamNonBlocking) == cudaSuccess;
     for (int s = 0; ok && s < kSlots; ++s) {
         ok = cudaHostAlloc(&w->host[s], slot_bytes, cudaHostAllocDefault) == cudaSuccess &&
@@ -137,6 +154,7 @@ cc3d_status cc3d_writer_submit(cc3d_writer_t w, const void* src, size_t bytes, v
         return CC3D_ERR_NOT_DEVICE_MEMORY;
     }
     if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return CC3D_ERR_NOT_DEVICE_MEMORY;
+    if (a.type == cudaMemoryTypeDevice && a.device != w->device) return CC3D_ERR_INVALID_ARG;
     long long seq;
     int slot;
     {

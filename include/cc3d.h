@@ -47,6 +47,9 @@
  *    cc3d_get_status synchronises the host.
  *  - Every argument is checked before anything is launched or written; a
  *    failed check returns an error code and leaves every buffer untouched.
+ *    Device pointers must belong to the device current at the call (or be
+ *    managed memory): host memory gives CC3D_ERR_NOT_DEVICE_MEMORY, another
+ *    device's memory CC3D_ERR_INVALID_ARG.
  *  - Kernel waits are bounded.  A wait that runs out records an error in a
  *    per-device status word and the kernel returns; cc3d_get_status reports
  *    it.
@@ -179,9 +182,12 @@ cc3d_status cc3d_forward_chunk_u8(cc3d_plan_t plan, int T_chunk, const void* x_c
  *   block) until the copy of submission `seq` is done.  seq < 0 is a no-op.
  * cc3d_writer_close: writes everything submitted, stops the worker, frees the writer
  *   (also on error); *bytes_written (may be NULL) receives the bytes written.
- * Errors: CC3D_ERR_INVALID_ARG, CC3D_ERR_NOT_DEVICE_MEMORY (src), CC3D_ERR_CUDA,
- * CC3D_ERR_OOM, CC3D_ERR_IO (open or write failed; reported by the next submit and
- * by close).  A writer is used from one host thread at a time.
+ * Errors: CC3D_ERR_INVALID_ARG (also: src on another device than the one current at
+ * create), CC3D_ERR_NOT_DEVICE_MEMORY (src), CC3D_ERR_CUDA, CC3D_ERR_OOM, CC3D_ERR_IO
+ * (open or write failed; reported by the next submit and by close).  After the first
+ * failed copy or write, the chunks still queued are dropped, not written: the file
+ * holds the chunks before the failure and nothing after it.  A writer is used from
+ * one host thread at a time.
  */
 cc3d_status cc3d_writer_create(const char* path, size_t slot_bytes, cc3d_writer_t* out);
 cc3d_status cc3d_writer_submit(cc3d_writer_t w, const void* src, size_t bytes, void* compute_stream,
@@ -194,7 +200,11 @@ cc3d_status cc3d_writer_close(cc3d_writer_t w, long long* bytes_written);
 cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream);
 
 /* Synchronise the stream, then report (and clear) the device status word and
- * any pending CUDA error: CC3D_OK, CC3D_ERR_DEVICE_TIMEOUT or CC3D_ERR_CUDA. */
+ * any pending CUDA error: CC3D_OK, CC3D_ERR_DEVICE_TIMEOUT or CC3D_ERR_CUDA.
+ * The word is read and cleared in one atomic exchange on the device (a bit set
+ * meanwhile by a kernel still running elsewhere is kept for the next call).  It
+ * is one word per device, shared by every plan on it: a timeout in one plan's
+ * kernel is reported to whichever caller polls that device first. */
 cc3d_status cc3d_get_status(cc3d_plan_t plan, void* stream);
 
 /* Release the plan (NULL is accepted). */
@@ -245,6 +255,36 @@ cc3d_status cc3d_plan_describe(cc3d_plan_t plan, int T_chunk, int has_residual, 
  */
 cc3d_status cc3d_debug_set_wait_budget_ns(cc3d_plan_t plan, unsigned long long ns);
 cc3d_status cc3d_debug_set_fault(cc3d_plan_t plan, int mode);
+
+/*
+ * Schedule overrides of the bf16 tensor-core families "tc_bf16", "tc_bf16_pair",
+ * "tc_bf16_narrow" and "tc_bf16_up2" (for tuning sweeps and for the tests that
+ * compare two schedules bit for bit; never needed in normal use).  Every knob
+ * starts at -1, the measured default for the chunk's shape.  A knob changes only
+ * how the work is tiled: the accumulation order of every output is fixed, so
+ * every schedule gives the same bits.  A combination with no configuration makes
+ * cc3d_forward_chunk return CC3D_ERR_UNSUPPORTED (nothing launched); one whose
+ * shared memory does not fit the SM is refused by the launch (CC3D_ERR_CUDA).
+ * The plan's settings are its own: nothing is read from the environment.
+ * cc3d_debug_set_schedule returns CC3D_ERR_INVALID_ARG for a NULL plan, an
+ * unknown knob or a value outside the knob's range (given beside it; -1 restores
+ * the default).
+ */
+typedef enum {
+    CC3D_SCHED_PAIR = 0,           /* 0..1: SM pairs (cta_group::2) where the geometry allows */
+    CC3D_SCHED_TWO_FRAME = 1,      /* 0..1: two output frames per MMA on SM pairs (chunks of >= 2 frames) */
+    CC3D_SCHED_SPLIT_TAIL = 2,     /* 0..1: split the tiles of a short last wave between both MMA warps */
+    CC3D_SCHED_CHANNEL_BLOCKS = 3, /* 0..1: outputs wider than 256 channels as channel-block tiles */
+    CC3D_SCHED_MMA_WARPS = 4,      /* 1..2: MMA-issuing warps */
+    CC3D_SCHED_ROW_GROUPS = 5,     /* 1, 2 or 4: 128-row groups per tile */
+    CC3D_SCHED_ACC_STAGES = 6,     /* 1..2: accumulator buffers in tensor memory */
+    CC3D_SCHED_TAP_ROWS = 7,       /* 1 or 3: kernel rows per weight stage */
+    CC3D_SCHED_WINDOW_STAGES = 8,  /* 2..8: input-window ring depth */
+    CC3D_SCHED_WEIGHT_STAGES = 9,  /* 2..8: upper bound of the weight ring depth */
+    CC3D_SCHED_PREFETCH = 10,      /* 0..3: temporal taps of the next tile warmed in L2 */
+    CC3D_SCHED_COUNT = 11
+} cc3d_schedule_knob;
+cc3d_status cc3d_debug_set_schedule(cc3d_plan_t plan, int knob, int value);
 
 #ifdef __cplusplus
 }

@@ -2,8 +2,9 @@
 
 This module holds the input generators and nothing of the convolution's
 arithmetic.  It is the one place both sides of a parity check draw their
-inputs from: the CPU side here (numpy), the GPU side in ``synth_gpu.cu``
-(loaded through ``synth.gpu``), both implementing the same counter-based
+inputs from: the CPU side here (numpy, and a C copy of it in ``synth_kernels.cu``'s host
+code), the GPU side in the fill kernel of ``synth_kernels.cu`` (loaded through
+``synth.native``), all implementing the same counter-based
 definition so that every element is a pure function of
 (seed, tensor id, global element index) and therefore independent of how a
 video is split into chunks or of which device produced it.

@@ -343,3 +343,74 @@ def test_a_plain_c_program_compiles_links_and_calls_the_library(lib, tmp_path):
     assert out[0] == "tc_bf16_pair"
     assert out[1].startswith("kernel=tc2s_bf16_kernel ")
     assert out[2] == "forward without buffers: 1"
+
+
+def test_schedule_knobs_are_validated_and_plan_local(lib):
+    p = cc3d.cc3d_plan_create(96, 96, 360, 640, 3, 3, 3, cc3d.CC3D_BF16)
+    q = cc3d.cc3d_plan_create(96, 96, 360, 640, 3, 3, 3, cc3d.CC3D_BF16)
+    try:
+        f = lib.cc3d_debug_set_schedule
+        assert f(None, 0, 1) == 1                              # null plan
+        assert f(p, -1, 0) == 1 and f(p, 11, 0) == 1           # unknown knobs
+        for knob, bad in ((0, 2), (1, -2), (4, 3), (5, 3), (5, 8), (6, 3), (7, 2), (8, 1), (9, 9), (10, 4)):
+            assert f(p, knob, bad) == 1, (knob, bad)
+        assert cc3d.cc3d_plan_describe(p, 4)["kernel"] == "tc2s_bf16_kernel"
+        cc3d.cc3d_debug_set_schedule(p, "two_frame", 0)
+        assert cc3d.cc3d_plan_describe(p, 4)["kernel"] == "tc2_bf16_kernel"
+        cc3d.cc3d_debug_set_schedule(p, "pair", 0)
+        assert cc3d.cc3d_plan_describe(p, 4)["kernel"] == "tc_bf16_kernel"
+        # another plan of the same shape keeps its defaults
+        assert cc3d.cc3d_plan_describe(q, 4)["kernel"] == "tc2s_bf16_kernel"
+        cc3d.cc3d_debug_set_schedule(p, "pair", -1)
+        cc3d.cc3d_debug_set_schedule(p, "two_frame", -1)
+        assert cc3d.cc3d_plan_describe(p, 4) == cc3d.cc3d_plan_describe(q, 4)
+        # a combination with no configuration is refused when the chunk is described (or run)
+        # (SM pairs hold at most two 128-row groups per block)
+        cc3d.cc3d_debug_set_schedule(p, "row_groups", 4)
+        with pytest.raises(cc3d.CC3DError) as e:
+            cc3d.cc3d_plan_describe(p, 1)
+        assert e.value.code == 2
+    finally:
+        cc3d.cc3d_destroy(p)
+        cc3d.cc3d_destroy(q)
+
+
+def test_launch_configuration_ignores_the_environment(lib):
+    """The library reads no environment variable: a process that carries old tuning variables
+    gets the measured configuration."""
+    import subprocess
+    import sys
+    code = ("import json, chunked_causal_convolution_gb300 as c;"
+            "p = c.cc3d_plan_create(96, 96, 360, 640); print(json.dumps(c.cc3d_plan_describe(p, 4)))")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root)
+    plain = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True)
+    env.update({"CC3D_TC_PAIR": "0", "CC3D_TC_TSTACK": "0", "CC3D_TC_NA": "5", "CC3D_TC_RB": "1",
+                "CC3D_TC_SUB": "1"})
+    tuned = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True)
+    assert plain.stdout == tuned.stdout and "tc2s_bf16_kernel" in plain.stdout
+    src = os.path.join(root, "chunked_causal_convolution_gb300", "csrc")
+    for name in os.listdir(src):
+        assert "getenv" not in open(os.path.join(src, name)).read(), name
+
+
+def test_binding_refuses_a_tensor_of_another_device(monkeypatch):
+    """A CUDA tensor on another device than the current one is refused before any pointer reaches
+    the library (the C ABI compares the pointer's device with the current one as well)."""
+    import torch
+
+    class FakeCudaTensor:
+        is_cuda = True
+        device = torch.device("cuda", 1)
+
+        def is_contiguous(self):
+            return True
+
+        def data_ptr(self):
+            return 0x10000
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    with pytest.raises(ValueError, match="current device"):
+        cc3d._addr(FakeCudaTensor())
+    FakeCudaTensor.device = torch.device("cuda", 0)
+    assert cc3d._addr(FakeCudaTensor()) == 0x10000

@@ -3,9 +3,8 @@ cc3d_plan_describe.
 
 Every template instantiation of the tensor-core kernels that some supported layer can launch is
 listed. The test checks that the GPU parity cases (tests/test_parity_gpu.py,
-tests/test_graph_gpu.py and the full-size workloads) launch each one, except the gaps named
-below. A change that makes a new instantiation reachable fails here until a GPU case covers it.
-A gap that gets covered can be removed from the list.
+tests/test_graph_gpu.py and the full-size workloads) launch each one.  A change that makes a new
+instantiation reachable fails here until a GPU case covers it.
 """
 import itertools
 
@@ -17,16 +16,9 @@ from chunked_causal_convolution_gb300 import build as lib_build
 from tests import test_parity_gpu as tp
 from tests.helpers import compositions_sample
 
-# Reachable with 16-channel blocks (Cin an odd multiple of 16) or a 4-channel head, but not yet
-# launched by any GPU parity case.
-KNOWN_GAPS = {
-    ("tc2_bf16_kernel", 16, 3),    # SM pairs on row-aligned frames (W a multiple of 128), e.g. 16 -> 32
-    ("tc2s_bf16_kernel", 16, 3),   # the same with chunks of two or more frames
-    ("tc_bf16_kernel", 16, 1, 1),  # one SM, one row group per MMA warp, 1-tap rows, e.g. 16 -> 192
-    ("tc_bf16_kernel", 16, 1, 3),  # fused upsample, one row group, e.g. 16 -> 96
-    ("tc_bf16_kernel", 16, 4, 3),  # fused upsample, four row groups, e.g. 16 -> 16
-    ("head_bf16_kernel", 4),       # narrow head with four output channels
-}
+# Reachable kernel instantiations that no GPU parity case launches yet: none.  (The 16-channel-block
+# SM-pair, one-SM and fused-upsample instantiations and the 4-channel head have their own cases.)
+KNOWN_GAPS = set()
 
 
 def instantiation(d, Cout):

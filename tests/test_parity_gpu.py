@@ -52,6 +52,13 @@ SMALL = [
     ("bf16_c96_wide_flat_window", "bf16", 96, 96, 3, 8, 100, [2, 1], True, True),
     ("bf16_c256_narrow_column_blocks", "bf16", 256, 256, 2, 3, 254, [1, 1], True, False),
     ("bf16_one_pixel", "bf16", 32, 32, 3, 1, 1, [1, 1, 1], True, True),
+    # 16-channel blocks (Cin an odd multiple of 16) on SM pairs over row-aligned frames: the
+    # two-frame schedule for the 4-frame chunk, the one-frame schedule for the 1-frame chunk
+    ("bf16_cb16_pairs_row_aligned", "bf16", 48, 96, 5, 3, 256, [4, 1], True, True),
+    # 16-channel blocks on one SM with one row group per MMA warp and 3-tap weight stages
+    ("bf16_cb16_one_sm_wide_n", "bf16", 16, 192, 3, 5, 40, [2, 1], True, False),
+    # a 4-channel narrow head
+    ("bf16_head_cout4", "bf16", 96, 4, 4, 5, 140, [3, 1], True, True),
 ]
 
 
@@ -64,6 +71,8 @@ SMALL_KERNEL = {
     "bf16_head_cout2": "tc_bf16_head", "bf16_narrow_generic": "tc_bf16_narrow", "bf16_cb16": "tc_bf16",
     "bf16_two_flat_blocks": "tc_bf16", "bf16_c192_like": "tc_bf16", "bf16_one_pixel": "tc_bf16",
     "bf16_c96_wide_flat_window": "tc_bf16", "bf16_c256_narrow_column_blocks": "tc_bf16",
+    "bf16_cb16_pairs_row_aligned": "tc_bf16_pair", "bf16_cb16_one_sm_wide_n": "tc_bf16",
+    "bf16_head_cout4": "tc_bf16_head",
 }
 
 
@@ -454,6 +463,10 @@ UP2 = [
     ("up2_cout192_blocks", 32, 192, 3, 3, 20, [3], True, True, 3),
     ("up2_spatial_only", 32, 32, 2, 6, 70, [1, 1], True, False, 1),
     ("up2_kt2_wide_rows", 32, 64, 3, 2, 128, [2, 1], False, True, 2),
+    # 16-channel blocks: one row group of four 96-channel classes, and four row groups of
+    # 16-channel classes
+    ("up2_cb16_c96", 16, 96, 3, 4, 40, [2, 1], True, True, 3),
+    ("up2_cb16_c16", 16, 16, 3, 5, 70, [1, 2], True, False, 3),
 ]
 
 
@@ -513,9 +526,9 @@ TSTACK = [
 
 
 @pytest.mark.parametrize("case", TSTACK, ids=[c[0] for c in TSTACK])
-def test_two_frame_pair_schedule_is_bit_identical_to_the_one_frame_schedule(case, monkeypatch):
+def test_two_frame_pair_schedule_is_bit_identical_to_the_one_frame_schedule(case):
     """Chunks of two or more frames on SM pairs stack two output frames into N; the one-frame pair
-    schedule (chosen for 1-frame chunks, or forced here through the tuning variable) accumulates
+    schedule (chosen for 1-frame chunks, or forced here through the plan's schedule knob) accumulates
     every output in the same order, so the two agree bit for bit, and both match the oracle."""
     name, Cin, Cout, T, H, W, chunks, bias, residual, kt = case
     raw = small_inputs(Cin, Cout, T, H, W, "bf16", 300 + len(name), bias, residual, k=(kt, 3, 3))
@@ -524,10 +537,11 @@ def test_two_frame_pair_schedule_is_bit_identical_to_the_one_frame_schedule(case
     assert plan.kernel == "tc_bf16_pair"
     y2, c2 = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), chunks)
     assert plan.status() == 0
-    monkeypatch.setenv("CC3D_TC_TSTACK", "0")
+    plan.set_schedule("two_frame", 0)
+    assert plan.describe(chunks[0], residual)["kernel"] == "tc2_bf16_kernel"
     y1, c1 = run_chunks(plan, dev["x"], dev["w"], dev.get("b"), dev.get("r"), chunks)
     assert plan.status() == 0
-    monkeypatch.delenv("CC3D_TC_TSTACK")
+    plan.set_schedule("two_frame", -1)
     assert torch.equal(y2, y1), name
     for a, b in zip(c2, c1):
         assert torch.equal(a, b), name
@@ -583,7 +597,7 @@ def test_outputs_and_residual_only_16_byte_aligned(case):
 
 @pytest.mark.parametrize("shape", [(192, 192, 5, 6, 64), (384, 192, 4, 5, 40), (64, 256, 3, 7, 100)],
                          ids=["c192_like", "c384_to_192_like", "c64_to_256"])
-def test_split_tail_tiles_are_bit_identical(shape, monkeypatch):
+def test_split_tail_tiles_are_bit_identical(shape):
     """A short last wave of two-row-group tiles is split into one-row-group units that both MMA
     warps compute, on half of the output channels each (at these sizes every tile is split).
     Each output keeps its MMAs and their order, so the result equals the unsplit launch bit for
@@ -595,10 +609,10 @@ def test_split_tail_tiles_are_bit_identical(shape, monkeypatch):
     assert plan.kernel == "tc_bf16"
     y_split, c_split = run_chunks(plan, dev["x"], dev["w"], dev["b"], dev["r"], [T - 1, 1])
     assert plan.status() == 0
-    monkeypatch.setenv("CC3D_TC_SPLIT", "0")
+    plan.set_schedule("split_tail", 0)
     y_whole, c_whole = run_chunks(plan, dev["x"], dev["w"], dev["b"], dev["r"], [T - 1, 1])
     assert plan.status() == 0
-    monkeypatch.delenv("CC3D_TC_SPLIT")
+    plan.set_schedule("split_tail", -1)
     assert torch.equal(y_split, y_whole)
     assert all(torch.equal(a, b) for a, b in zip(c_split, c_whole))
     ref = oracle.conv_whole(to_f64(raw["x"], "bf16"), to_f64(raw["w"], "bf16"), to_f64(raw["b"], "bf16"),

@@ -7,7 +7,15 @@ tensor-core kernel (implicit-GEMM conv + bias + residual epilogue + cache
 update).  Inputs are resident in HBM before the timed region and larger than
 L2.  Prints one JSON line (rank 0).
 
+The same line carries, under "configs", the other decoder stages of the target
+(c192, c384, c384_to_192: the same 6 x 4-frame step, warm-up and timing, each
+with its clocks) and "sr_stream": the 4x super-resolution stage (the 96 -> 96
+conv, then the 96 -> 3 head on its output) over all 361 frames of 1440 x 2560
+in 90 chunks of 4 and one of 1.  Its "e2e" object adds the box's own pinned-copy
+floor for the step's host<->device bytes.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--no-configs] [--sr-passes P]
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload (host cores), printing the same metric.
@@ -234,12 +242,296 @@ def run_reference(args, wl):
 
 # ---------------------------------------------------------------- GPU arm
 
-def run_ours(args, wl):
+def _dominant_bound(wl, c_full, frame_in, frame_out, has_res, p):
+    """Bound of a full-chunk launch of the layer, its FLOPs and algorithmic bytes: tensor cores
+    unless its arithmetic intensity (history in and out included) is below the ridge."""
+    flop_per_launch = wl.flops / wl.T * c_full
+    bytes_per_launch = (c_full * frame_in + c_full * frame_out * (2 if has_res else 1)
+                        + 2 * (wl.kt - 1) * frame_in)
+    ridge = float(p["bf16_tflops"]) * 1e12 / (float(p["hbm_gbs"]) * 1e9)
+    return flop_per_launch, bytes_per_launch, flop_per_launch / bytes_per_launch < ridge
+
+
+def measure_layer(wl, args, dev, dist, local, world, keep=False):
+    """One layer's bench step (its chunk loop, histories ping-ponged) on resident inputs: W warm-up
+    steps, then K timed steps with CUDA events on the launching stream, a per-launch event pair
+    around every chunk, and the SM clocks sampled meanwhile.  Returns the measurements (and, with
+    keep, the tensors and plan for the end-to-end leg)."""
     import torch
 
     import chunked_causal_convolution_gb300 as cc3d
     import synth
     from synth import native
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    dt = torch.bfloat16
+    T, H, W = wl.T, wl.H, wl.W
+    Ho, Wo = wl.out_hw  # output frames (2H x 2W for an upsampling layer)
+    x = native.fill_device(torch.empty((T, H, W, wl.Cin), dtype=dt, device=dev), wl.seed, synth.TID_X, wl.x)
+    wt = native.fill_device(torch.empty((wl.Cout, wl.kt, wl.kh, wl.kw, wl.Cin), dtype=dt, device=dev), wl.seed,
+                            synth.TID_W, wl.w)
+    b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device=dev), wl.seed, synth.TID_B, wl.b)
+    r = None
+    if wl.r is not None:
+        r = native.fill_device(torch.empty((T, Ho, Wo, wl.Cout), dtype=dt, device=dev), wl.seed, synth.TID_R, wl.r)
+    y = torch.empty((T, Ho, Wo, wl.Cout), dtype=dt, device=dev)
+    if wl.up2:
+        plan = cc3d.Upsample2xConvPlan(wl.Cin, wl.Cout, H, W, wl.kt, dtype="bf16")
+    else:
+        plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, H, W, wl.kt, wl.kh, wl.kw, dtype="bf16")
+    caches = [plan.new_cache(dev), plan.new_cache(dev)]
+    stream = torch.cuda.Stream(device=dev)
+    bounds = []
+    s = 0
+    for c in wl.chunks:
+        bounds.append((s, c))
+        s += c
+
+    def step(ev_pairs=None):
+        for k, (s0, c) in enumerate(bounds):
+            if ev_pairs is not None:
+                ev_pairs[k][0].record(stream)
+            cc3d.cc3d_forward_chunk(plan.handle, c, x[s0:s0 + c], wt, b, r[s0:s0 + c] if r is not None else None,
+                                    caches[k % 2] if k else None, caches[(k + 1) % 2], y[s0:s0 + c], stream)
+            if ev_pairs is not None:
+                ev_pairs[k][1].record(stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    st = plan.status(stream)
+    if st != 0:
+        raise RuntimeError("%s: device status after warm-up: %s" % (wl.name, cc3d.cc3d_status_string(st)))
+
+    # ---- timed region: K steps, events on the launching stream
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launch_evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in bounds] for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.25)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                step(launch_evs[i])
+            end.record(stream)
+        stream.synchronize()
+        time.sleep(0.25)
+    barrier()
+    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
+    st = plan.status(stream)
+    if st != 0:
+        raise RuntimeError("%s: device status after timing: %s" % (wl.name, cc3d.cc3d_status_string(st)))
+    ms_per_step = ms / args.steps
+    value = wl.flops * world * args.steps / (ms / 1e3) / 1e12
+    # per-step durations (first launch start to last launch end of each step) and algorithmic bytes
+    step_ms = sorted(row[0][0].elapsed_time(row[-1][1]) for row in launch_evs)
+    step_stats = {"min": step_ms[0], "mean": sum(step_ms) / len(step_ms),
+                  "p99": step_ms[min(len(step_ms) - 1, int(round(0.99 * (len(step_ms) - 1))))]}
+    frame_in, frame_out = H * W * wl.Cin * 2, Ho * Wo * wl.Cout * 2
+    bytes_per_step = 0
+    for k, (_, c) in enumerate(bounds):
+        bytes_per_step += c * frame_in + c * frame_out * (2 if r is not None else 1)  # x, y (+ residual)
+        bytes_per_step += ((wl.kt - 1) * frame_in if k else 0) + (wl.kt - 1) * frame_in  # history read, written
+    p, src = peaks()
+    hbm_gbs = bytes_per_step * world / (ms_per_step / 1e3) / 1e9
+    # per-launch durations of the dominant (only) kernel
+    launch_ms = [a.elapsed_time(bb) for row in launch_evs for (a, bb) in row]
+    c_full = max(wl.chunks)
+    full = [ms_ for ms_, (_, c) in zip(launch_ms, bounds * args.steps) if c == c_full]
+    avg_launch_ms = sum(full) / len(full)
+    flop_per_launch, bytes_per_launch, hbm_bound = _dominant_bound(wl, c_full, frame_in, frame_out, r is not None, p)
+    if hbm_bound:
+        achieved = bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
+        peak = float(p["hbm_gbs"])
+    else:
+        achieved = flop_per_launch / (avg_launch_ms / 1e3) / 1e12
+        peak = float(p["bf16_tflops"])
+    peak_note = "%s MEASURED_PEAKS %s" % (src, "hbm_gbs (copy bandwidth)" if hbm_bound else
+                                           "bf16_tflops (burst, kernel timed alone)")
+    out = {
+        "value": value, "ms_per_step": ms_per_step, "kernel": plan.kernel,
+        "dominant_kernel": plan.describe(c_full, r is not None).get("kernel"),
+        "output_frames_per_s": wl.T * world * args.steps / (ms / 1e3),
+        "pct_of_dense_bf16_peak": {"measured_burst": 100 * value / world / float(p["bf16_tflops"]),
+                                   "measured_sustained": 100 * value / world / float(p["bf16_tflops_sustained"]),
+                                   "spec_2250": 100 * value / world / 2250.0},
+        "roofline": {"bound": "hbm" if hbm_bound else "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s" if hbm_bound else "TFLOP/s", "frac": achieved / peak,
+                     "traffic": traffic_per_launch(wl.name), "peak_source": peak_note, "kernel": plan.kernel,
+                     "flop_per_launch": flop_per_launch, "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "avg_launch_ms": avg_launch_ms},
+        "avg_launch_ms": avg_launch_ms,
+        "clocks": clocks.summary(),
+        "step_ms": step_stats,
+        "hbm": {"achieved_gbs": hbm_gbs, "peak_gbs": float(p["hbm_gbs"]),
+                "frac": hbm_gbs / world / float(p["hbm_gbs"]), "algorithmic_bytes_per_step": bytes_per_step},
+        "gpu_launches": args.steps * len(bounds) * plan.launches_per_chunk,
+    }
+    if keep:
+        out["_ctx"] = dict(x=x, wt=wt, b=b, r=r, y=y, plan=plan, caches=caches, stream=stream, bounds=bounds)
+    else:
+        plan.close()
+        del x, wt, b, r, y, caches
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
+def measure_sr_stream(args, dev, local):
+    """The 4x super-resolution output stage as a stream: the 96 -> 96 3x3x3 conv and the 96 -> 3
+    head after it, over all 361 frames of 1440 x 2560 in 90 chunks of 4 and a last chunk of 1, both
+    histories carried by the library from chunk to chunk, the head reading the conv's output.
+    Inputs: a ring of two 4-frame chunks (the video's frames 0-3 and 4-7, generated on the device
+    before the timed region) that chunk k reads in turn (k mod 2), so the 255 GB video never has
+    to be resident; the work per chunk is the same.  One untimed pass, then `args.sr_passes`
+    timed passes back to back (CUDA events around each pass and around every launch)."""
+    import torch
+
+    import chunked_causal_convolution_gb300 as cc3d
+    import synth
+    from synth import native
+
+    conv_wl, head_wl = synth.WORKLOADS["sr96"], synth.WORKLOADS["sr_head3"]
+    H, W, C = conv_wl.H, conv_wl.W, conv_wl.Cin
+    dt = torch.bfloat16
+    frame = H * W * C
+    ring = [native.fill_device(torch.empty((4, H, W, C), dtype=dt, device=dev), conv_wl.seed, synth.TID_X, conv_wl.x,
+                               offset=4 * j * frame) for j in range(2)]
+    w1 = native.fill_device(torch.empty((96, 3, 3, 3, C), dtype=dt, device=dev), conv_wl.seed, synth.TID_W, conv_wl.w)
+    b1 = native.fill_device(torch.empty((96,), dtype=dt, device=dev), conv_wl.seed, synth.TID_B, conv_wl.b)
+    w2 = native.fill_device(torch.empty((3, 3, 3, 3, C), dtype=dt, device=dev), head_wl.seed, synth.TID_W, head_wl.w)
+    b2 = native.fill_device(torch.empty((3,), dtype=dt, device=dev), head_wl.seed, synth.TID_B, head_wl.b)
+    conv = cc3d.CausalConv3dPlan(C, 96, H, W)
+    head = cc3d.CausalConv3dPlan(96, 3, H, W)
+    c1 = [conv.new_cache(dev), conv.new_cache(dev)]
+    c2 = [head.new_cache(dev), head.new_cache(dev)]
+    y1 = torch.empty((4, H, W, 96), dtype=dt, device=dev)
+    y2 = torch.empty((4, H, W, 3), dtype=dt, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    chunks = list(conv_wl.chunks)
+
+    def one_pass(evs=None):
+        for k, c in enumerate(chunks):
+            if evs is not None:
+                evs[k][0].record(stream)
+            cc3d.cc3d_forward_chunk(conv.handle, c, ring[k % 2][:c], w1, b1, None, c1[k % 2] if k else None,
+                                    c1[(k + 1) % 2], y1[:c], stream)
+            if evs is not None:
+                evs[k][1].record(stream)
+            cc3d.cc3d_forward_chunk(head.handle, c, y1[:c], w2, b2, None, c2[k % 2] if k else None,
+                                    c2[(k + 1) % 2], y2[:c], stream)
+            if evs is not None:
+                evs[k][2].record(stream)
+
+    with torch.cuda.stream(stream):
+        one_pass()
+    for plan in (conv, head):
+        st = plan.status(stream)
+        if st != 0:
+            raise RuntimeError("sr stream: device status after warm-up: %s" % cc3d.cc3d_status_string(st))
+    passes = max(1, args.sr_passes)
+    evs = [[tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in chunks] for _ in range(passes)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.25)
+        with torch.cuda.stream(stream):
+            for i in range(passes):
+                one_pass(evs[i])
+        stream.synchronize()
+        time.sleep(0.25)
+    for plan in (conv, head):
+        st = plan.status(stream)
+        if st != 0:
+            raise RuntimeError("sr stream: device status after timing: %s" % cc3d.cc3d_status_string(st))
+    pass_ms = [e[0][0].elapsed_time(e[-1][2]) for e in evs]
+    conv_ms = [e[k][0].elapsed_time(e[k][1]) for e in evs for k, c in enumerate(chunks) if c == 4]
+    head_ms = [e[k][1].elapsed_time(e[k][2]) for e in evs for k, c in enumerate(chunks) if c == 4]
+    p, src = peaks()
+    flops_conv, flops_head = conv_wl.flops, head_wl.flops
+    total_s = sum(pass_ms) / 1e3
+    conv_launch = sum(conv_ms) / len(conv_ms)
+    head_launch = sum(head_ms) / len(head_ms)
+    conv_tflops = flops_conv / conv_wl.T * 4 / (conv_launch / 1e3) / 1e12
+    # the head's algorithmic bytes per 4-frame launch: x read, 2-frame history read and written, y
+    head_bytes = 4 * H * W * C * 2 + 2 * 2 * H * W * C * 2 + 4 * H * W * 3 * 2
+    head_gbs = head_bytes / (head_launch / 1e3) / 1e9
+    out = {
+        "workload": "sr_stream: 4x super-resolution output stage, causal conv3d 96->96 3x3x3 (bias) then the "
+                    "96->3 3x3x3 head (bias) on its output, 361 frames of 1440x2560 in 90 chunks of 4 + 1 of 1, "
+                    "both 2-frame histories carried through the library, batch 1",
+        "inputs": "ring of two 4-frame input chunks (frames 0-3 and 4-7 of the seeded video, generated on the "
+                  "device before the timed region), chunk k reads ring[k mod 2]; 2.83 GB per chunk (larger than L2)",
+        "passes": passes, "ms_per_pass": total_s * 1e3 / passes,
+        "value": (flops_conv + flops_head) * passes / total_s / 1e12, "unit": UNIT,
+        "output_frames_per_s": conv_wl.T * passes / total_s,
+        "flop_per_pass": flops_conv + flops_head,
+        # a pass lasts about half a second under the power cap: the sustained peak is the
+        # denominator (the burst fraction beside it)
+        "conv": {"kernel": conv.describe(4, False).get("kernel"), "avg_launch_ms": conv_launch,
+                 "tflops": conv_tflops, "frac": conv_tflops / float(p["bf16_tflops_sustained"]),
+                 "peak": float(p["bf16_tflops_sustained"]),
+                 "peak_source": src + " MEASURED_PEAKS bf16_tflops_sustained (kernel inside a long step)",
+                 "frac_of_burst": conv_tflops / float(p["bf16_tflops"])},
+        "head": {"kernel": head.describe(4, False).get("kernel"), "avg_launch_ms": head_launch,
+                 "algorithmic_bytes_per_launch": head_bytes, "achieved_gbs": head_gbs,
+                 "frac_of_hbm": head_gbs / float(p["hbm_gbs"]), "peak_gbs": float(p["hbm_gbs"]),
+                 "peak_source": src + " MEASURED_PEAKS hbm_gbs (copy bandwidth)"},
+        "clocks": clocks.summary(),
+        "gpu_launches": passes * 2 * len(chunks),
+    }
+    conv.close()
+    head.close()
+    del ring, y1, y2, c1, c2
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def copy_bound(xh, rh, yh, x, r, y, dev, reps=3):
+    """The box's own pinned-copy floor for the end-to-end step's bytes: the step's host->device
+    bytes (x, then the residual) on one stream and its device->host bytes (y) on another, each as
+    whole-tensor cudaMemcpyAsync calls, both directions at once; also each direction alone.  Best of
+    `reps` (milliseconds)."""
+    import torch
+
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(h2d, d2h):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_in)
+            s_out.wait_event(e0)
+            if h2d:
+                with torch.cuda.stream(s_in):
+                    x.copy_(xh, non_blocking=True)
+                    if rh is not None:
+                        r.copy_(rh, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s_out):
+                    yh.copy_(y, non_blocking=True)
+            s_in.wait_stream(s_out)
+            e1.record(s_in)
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1)
+            best = t if best is None else min(best, t)
+        return best
+
+    return {"both_ms": timed(True, True), "h2d_only_ms": timed(True, False), "d2h_only_ms": timed(False, True)}
+
+
+def run_ours(args, wl):
+    import torch
+
+    import chunked_causal_convolution_gb300 as cc3d
+    import synth
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -264,95 +556,10 @@ def run_ours(args, wl):
 
     dev = torch.device("cuda", local)
     dt = torch.bfloat16
-    T, H, W = wl.T, wl.H, wl.W
-    Ho, Wo = wl.out_hw  # output frames (2H x 2W for an upsampling layer)
-    x = native.fill_device(torch.empty((T, H, W, wl.Cin), dtype=dt, device=dev), wl.seed, synth.TID_X, wl.x)
-    wt = native.fill_device(torch.empty((wl.Cout, wl.kt, wl.kh, wl.kw, wl.Cin), dtype=dt, device=dev), wl.seed,
-                            synth.TID_W, wl.w)
-    b = native.fill_device(torch.empty((wl.Cout,), dtype=dt, device=dev), wl.seed, synth.TID_B, wl.b)
-    r = None
-    if wl.r is not None:
-        r = native.fill_device(torch.empty((T, Ho, Wo, wl.Cout), dtype=dt, device=dev), wl.seed, synth.TID_R, wl.r)
-    y = torch.empty((T, Ho, Wo, wl.Cout), dtype=dt, device=dev)
-    if wl.up2:
-        plan = cc3d.Upsample2xConvPlan(wl.Cin, wl.Cout, H, W, wl.kt, dtype="bf16")
-    else:
-        plan = cc3d.CausalConv3dPlan(wl.Cin, wl.Cout, H, W, wl.kt, wl.kh, wl.kw, dtype="bf16")
-    caches = [plan.new_cache(dev), plan.new_cache(dev)]
-    stream = torch.cuda.Stream(device=dev)
-    bounds = []
-    s = 0
-    for c in wl.chunks:
-        bounds.append((s, c))
-        s += c
-
-    def step(ev_pairs=None, xs=x, rs=r, ys=y):
-        for k, (s0, c) in enumerate(bounds):
-            if ev_pairs is not None:
-                ev_pairs[k][0].record(stream)
-            cc3d.cc3d_forward_chunk(plan.handle, c, xs[s0:s0 + c], wt, b,
-                                    rs[s0:s0 + c] if rs is not None else None,
-                                    caches[k % 2] if k else None, caches[(k + 1) % 2], ys[s0:s0 + c], stream)
-            if ev_pairs is not None:
-                ev_pairs[k][1].record(stream)
-
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    if plan.status(stream) != 0:
-        raise RuntimeError("device status after warm-up: %s" % cc3d.cc3d_status_string(plan.status(stream)))
-
-    # ---- timed region: K steps, events on the launching stream
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launch_evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in bounds] for _ in range(args.steps)]
-    barrier()
-    with ClockSampler(local) as clocks:
-        time.sleep(0.25)
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for i in range(args.steps):
-                step(launch_evs[i])
-            end.record(stream)
-        stream.synchronize()
-        time.sleep(0.25)
-    barrier()
-    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
-    st = plan.status(stream)
-    if st != 0:
-        raise RuntimeError("device status after timing: %s" % cc3d.cc3d_status_string(st))
-    ms_per_step = ms / args.steps
-    value = wl.flops * world * args.steps / (ms / 1e3) / 1e12
-    # per-step durations (first launch start to last launch end of each step) and algorithmic bytes
-    step_ms = sorted(row[0][0].elapsed_time(row[-1][1]) for row in launch_evs)
-    step_stats = {"min": step_ms[0], "mean": sum(step_ms) / len(step_ms),
-                  "p99": step_ms[min(len(step_ms) - 1, int(round(0.99 * (len(step_ms) - 1))))]}
-    frame_in, frame_out = H * W * wl.Cin * 2, Ho * Wo * wl.Cout * 2
-    bytes_per_step = 0
-    for k, (_, c) in enumerate(bounds):
-        bytes_per_step += c * frame_in + c * frame_out * (2 if r is not None else 1)  # x, y (+ residual)
-        bytes_per_step += ((wl.kt - 1) * frame_in if k else 0) + (wl.kt - 1) * frame_in  # history read, written
-    hbm_gbs = bytes_per_step * world / (ms_per_step / 1e3) / 1e9
-    # per-launch durations of the dominant (only) kernel
-    launch_ms = [a.elapsed_time(bb) for row in launch_evs for (a, bb) in row]
-    full = [ms_ for ms_, (_, c) in zip(launch_ms, bounds * args.steps) if c == max(wl.chunks)]
-    avg_launch_ms = sum(full) / len(full)
-    flop_per_launch = wl.flops / T * max(wl.chunks)
-    p, src = peaks()
-    # the bound of the dominant kernel: tensor cores unless its arithmetic intensity (FLOP per
-    # algorithmic byte of a full chunk launch, history in and out included) is below the ridge
-    c_full = max(wl.chunks)
-    bytes_per_launch = (c_full * frame_in + c_full * frame_out * (2 if r is not None else 1)
-                        + 2 * (wl.kt - 1) * frame_in)
-    hbm_bound = flop_per_launch / bytes_per_launch < float(p["bf16_tflops"]) * 1e12 / (float(p["hbm_gbs"]) * 1e9)
-    if hbm_bound:
-        achieved = bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
-        peak = float(p["hbm_gbs"])
-    else:
-        achieved = flop_per_launch / (avg_launch_ms / 1e3) / 1e12
-        peak = float(p["bf16_tflops"])
-    traffic = traffic_per_launch(wl.name)
+    m = measure_layer(wl, args, dev, dist, local, world, keep=True)
+    ctx = m.pop("_ctx")
+    x, wt, b, r, y, plan, caches, stream, bounds = (ctx[k] for k in ("x", "wt", "b", "r", "y", "plan", "caches",
+                                                                    "stream", "bounds"))
 
     # ---- end to end: pinned host inputs -> device -> chunk loop -> host result, every step.
     # Chunk k's host->device copy (copy stream), its conv (compute stream) and the device->host
@@ -408,14 +615,35 @@ def run_ours(args, wl):
         raise RuntimeError("end-to-end result differs from the device-resident result")
     h2d = x.numel() * 2 + (r.numel() * 2 if r is not None else 0)
     d2h = y.numel() * 2
+    cb = copy_bound(xh, rh, yh, x, r, y, dev)
+    e2e_step_ms = e2e_ms / args.steps
+    plan.close()
+    del x, r, y, xb, rb, yb, caches, ctx
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    # ---- the other decoder stages of the same target, each its own 6 x 4-frame step, and the
+    # super-resolution stage as a 361-frame stream
+    configs = {}
+    if not args.no_configs:
+        for name in ("c192", "c384", "c384_to_192"):
+            if name == wl.name:
+                continue
+            mc = measure_layer(synth.WORKLOADS[name], args, dev, dist, local, world)
+            configs[name] = {k: mc[k] for k in ("value", "ms_per_step", "output_frames_per_s", "avg_launch_ms",
+                                                "kernel", "dominant_kernel", "clocks", "gpu_launches")}
+            configs[name]["roofline"] = {k: mc["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+            configs[name]["config"] = workload_config(synth.WORKLOADS[name])
+        if world == 1:
+            configs["sr_stream"] = measure_sr_stream(args, dev, local)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         # whole output frames of the workload, repeated until about 10 s of CPU work
         flops, secs, reps = 0.0, 0.0, 0
         while secs < 10.0 and reps < 8:
-            f, dt, n = oracle_sample(wl, wl.H)
-            flops, secs, reps = flops + f, secs + dt, reps + 1
+            f, dt_, n = oracle_sample(wl, wl.H)
+            flops, secs, reps = flops + f, secs + dt_, reps + 1
         cpu = {"value": flops / secs / 1e12, "unit": UNIT, "cores": n, "kind": "oracle",
                "sample": "fp64 oracle chunk form: one whole output frame (frame %d, %dx%d) of %s from its "
                          "2-frame history, %d times (%.1f s)" % (wl.T // 2, wl.out_hw[0], wl.out_hw[1], wl.name, reps, secs)}
@@ -425,30 +653,27 @@ def run_ours(args, wl):
         dist.destroy_process_group()
     if rank != 0:
         return 0
-    peak_note = "%s MEASURED_PEAKS %s" % (src, "hbm_gbs (copy bandwidth)" if hbm_bound else
-                                           "bf16_tflops (burst, kernel timed alone)")
     out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator, on device)",
         "config": workload_config(wl),
-        "output_frames_per_s": wl.T * world * args.steps / (ms / 1e3),
-        "pct_of_dense_bf16_peak": {"measured_burst": 100 * value / world / float(p["bf16_tflops"]),
-                                   "measured_sustained": 100 * value / world / float(p["bf16_tflops_sustained"]),
-                                   "spec_2250": 100 * value / world / 2250.0},
-        "roofline": {"bound": "hbm" if hbm_bound else "tensor", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s" if hbm_bound else "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": peak_note, "kernel": plan.kernel, "flop_per_launch": flop_per_launch,
-                     "algorithmic_bytes_per_launch": bytes_per_launch, "avg_launch_ms": avg_launch_ms},
+        "output_frames_per_s": m["output_frames_per_s"],
+        "pct_of_dense_bf16_peak": m["pct_of_dense_bf16_peak"],
+        "roofline": m["roofline"],
         "cpu_baseline": cpu,
         "e2e": {"value": wl.flops * world * args.steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": args.steps * len(bounds) * plan.launches_per_chunk,
-        "clocks": clocks.summary(),
-        "step_ms": step_stats,
-        "hbm": {"achieved_gbs": hbm_gbs, "peak_gbs": float(p["hbm_gbs"]), "frac": hbm_gbs / world / float(p["hbm_gbs"]),
-                "algorithmic_bytes_per_step": bytes_per_step},
+                "ms_per_step": e2e_step_ms,
+                "copy_bound_ms": cb["both_ms"], "frac_of_copy_bound": cb["both_ms"] / e2e_step_ms,
+                "copy_bound": dict(cb, how="the step's H2D bytes (x, residual) and D2H bytes (y) as whole-tensor "
+                                           "pinned cudaMemcpyAsync calls, the two directions on two streams at "
+                                           "once; best of 3")},
+        "gpu_launches": m["gpu_launches"],
+        "clocks": m["clocks"],
+        "step_ms": m["step_ms"],
+        "hbm": m["hbm"],
+        "configs": configs,
     }
     print(json.dumps(out), flush=True)
     return 0
@@ -701,6 +926,9 @@ def main():
     ap.add_argument("--workload", default="c96_residual")
     ap.add_argument("--ref-rows", type=int, default=90, help="rows of the oracle sample frame")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only the headline workload (not the other decoder stages and the SR stream)")
+    ap.add_argument("--sr-passes", type=int, default=2, help="timed passes over the 361-frame SR stream")
     ap.add_argument("--single-chunk", type=int, default=0,
                     help="profiling case: run this many launches of one 4-frame chunk and exit")
     ap.add_argument("--output-path", default=None,

@@ -290,13 +290,21 @@ def measure_layer(wl, args, dev, dist, local, world, keep=False):
     for c in wl.chunks:
         bounds.append((s, c))
         s += c
+    # N > 1 ranks: the video is split along time, rank i owning frames [i*T, (i+1)*T); before its
+    # chunk loop every rank receives the kt - 1 input frames before its range from rank i - 1 (the
+    # causal halo exchange, NCCL point-to-point; zeros on rank 0) and its first chunk reads them
+    halo_hist = plan.new_cache(dev) if (dist is not None and wl.kt > 1) else None
 
     def step(ev_pairs=None):
+        first_hist = None
+        if halo_hist is not None:
+            from chunked_causal_convolution_gb300 import halo
+            first_hist = halo.exchange(x, wl.kt - 1, out=halo_hist)
         for k, (s0, c) in enumerate(bounds):
             if ev_pairs is not None:
                 ev_pairs[k][0].record(stream)
             cc3d.cc3d_forward_chunk(plan.handle, c, x[s0:s0 + c], wt, b, r[s0:s0 + c] if r is not None else None,
-                                    caches[k % 2] if k else None, caches[(k + 1) % 2], y[s0:s0 + c], stream)
+                                    caches[k % 2] if k else first_hist, caches[(k + 1) % 2], y[s0:s0 + c], stream)
             if ev_pairs is not None:
                 ev_pairs[k][1].record(stream)
 
@@ -356,6 +364,9 @@ def measure_layer(wl, args, dev, dist, local, world, keep=False):
                                            "bf16_tflops (burst, kernel timed alone)")
     out = {
         "value": value, "ms_per_step": ms_per_step, "kernel": plan.kernel,
+        "time_split": (None if halo_hist is None else
+                       "%d ranks, each %d frames; the %d-frame input history exchanged point-to-point before "
+                       "each step's chunk loop" % (world, T, wl.kt - 1)),
         "dominant_kernel": plan.describe(c_full, r is not None).get("kernel"),
         "output_frames_per_s": wl.T * world * args.steps / (ms / 1e3),
         "pct_of_dense_bf16_peak": {"measured_burst": 100 * value / world / float(p["bf16_tflops"]),

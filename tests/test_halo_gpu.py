@@ -1,0 +1,53 @@
+"""The time-split runner with the library's layers on one GPU (a single rank: the exchange is
+the hand-over of each layer's history from one wave to the next): a stack of layers run wave by
+wave through halo.TimeSplit equals the plain chunk loop over the whole video bit for bit (the
+library's result does not depend on where the video is cut), and the oracle within tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_causal_convolution_gb300 as cc3d
+import oracle
+from chunked_causal_convolution_gb300 import halo
+from tests.helpers import from_device, run_chunks, small_inputs, to_device, to_f64, tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def test_waves_through_the_time_split_equal_the_chunk_loop():
+    T, H, W = 11, 5, 128
+    spec = [(96, 96, 3), (96, 64, 2), (64, 3, 3)]  # SM-pair layer, MemoryBlock-like layer, narrow head
+    raw = small_inputs(96, 96, T, H, W, "bf16", 600, bias=True)
+    x = to_device(raw["x"], "bf16")
+    layers, plans, params = [], [], []
+    for j, (ci, co, kt) in enumerate(spec):
+        p = small_inputs(ci, co, 1, 1, 1, "bf16", 610 + j, bias=True, k=(kt, 3, 3))
+        w, b = to_device(p["w"], "bf16"), to_device(p["b"], "bf16")
+        plan = cc3d.CausalConv3dPlan(ci, co, H, W, kt, 3, 3)
+        plans.append(plan)
+        params.append((w, b, p))
+        layers.append(halo.ChunkedLayer(plan, w, b, chunk=4))
+    split = halo.TimeSplit(layers)
+    ys = [split.forward(x[a:b]) for a, b in ((0, 5), (5, 6), (6, 11))]
+    y_split = torch.cat(ys)
+    # the same stack, each layer as one chunk loop over the whole video
+    cur = x
+    for plan, (w, b, _) in zip(plans, params):
+        cur, _ = run_chunks(plan, cur, w, b, None, [4, 4, 3])
+    assert all(p.status() == 0 for p in plans)
+    assert torch.equal(y_split, cur)
+    ref = to_f64(raw["x"], "bf16")
+    for (w, b, p), plan in zip(params, plans):
+        ref = oracle.conv_whole(ref, to_f64(p["w"], "bf16"), to_f64(p["b"], "bf16"))
+        ref = oracle.round_bf16(ref)  # the next layer reads the bf16 values this layer stored
+    err = np.abs(from_device(y_split) - ref).max()
+    assert err <= tolerance("bf16", ref), err
+    for plan in plans:
+        plan.close()

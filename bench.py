@@ -854,6 +854,69 @@ def run_graph_timing(args, wl):
     return 0 if out["status"] == 0 else 1
 
 
+def run_layer_group(args, wl):
+    """Auxiliary measurement (one JSON line, not the bench line): the decoder's last three layers at
+    the c96 stage (two 96 -> 96 3x3x3 convs and the 96 -> 3 head, 360 x 640) over one 24-frame
+    chunk (the pages' chunk length) per step, run as a frame-batched layer group with batches of
+    1, 2 and 4 frames and as the whole chunk at once: time per chunk and the device memory the
+    step holds (inputs, outputs, histories and workspace; the peak of the caching allocator)."""
+    import torch
+
+    import __graft_entry__
+    import chunked_causal_convolution_gb300 as cc3d
+    import synth
+    from synth import native
+
+    __graft_entry__.build()
+    dt, T, H, W = torch.bfloat16, 24, 360, 640
+    base = synth.WORKLOADS["c96_residual"]
+    spec = [(96, 96), (96, 96), (96, 3)]
+    out = {"measurement": "frame-batched layer group", "layers": "96->96 3x3x3, 96->96 3x3x3, 96->3 3x3x3 at "
+           "360x640, bias", "chunk_frames": T, "steps": args.steps, "runs": {}}
+    for fb in (0, 1, 2, 4):
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats()
+        before = torch.cuda.memory_allocated()
+        plans = [cc3d.CausalConv3dPlan(ci, co, H, W) for ci, co in spec]
+        ws_ = [native.fill_device(torch.empty((co, 3, 3, 3, ci), dtype=dt, device="cuda"), base.seed + j,
+                                  synth.TID_W, synth.Dist.normal(synth.fan_in_sigma(ci))) for j, (ci, co) in enumerate(spec)]
+        bs_ = [native.fill_device(torch.empty((co,), dtype=dt, device="cuda"), base.seed + j, synth.TID_B,
+                                  base.b) for j, (ci, co) in enumerate(spec)]
+        x = native.fill_device(torch.empty((T, H, W, 96), dtype=dt, device="cuda"), base.seed, synth.TID_X, base.x)
+        y = torch.empty((T, H, W, 3), dtype=dt, device="cuda")
+        caches = [[p.new_cache(), p.new_cache()] for p in plans]
+        group = cc3d.LayerGroup(plans, fb)
+        ws = group.new_workspace(T)
+        s = torch.cuda.Stream()
+
+        def step(k):
+            group.forward_chunk(x, ws_, bs_, [c[k % 2] for c in caches] if k else None,
+                                [c[(k + 1) % 2] for c in caches], y, ws, stream=s)
+
+        with torch.cuda.stream(s):
+            for k in range(args.warmup):
+                step(k)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for k in range(args.steps):
+                step(k + 1)
+            e1.record(s)
+        s.synchronize()
+        st = [p.status(s) for p in plans]
+        out["runs"]["whole_chunk" if fb == 0 else "batch_%d" % fb] = {
+            "ms_per_chunk": e0.elapsed_time(e1) / args.steps, "workspace_bytes": group.workspace_bytes(T),
+            "peak_bytes": torch.cuda.max_memory_allocated() - before, "status": st}
+        group.close()
+        for p in plans:
+            p.close()
+        del x, y, caches, ws, ws_, bs_
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def run_upsample_compare(args, wl):
     """Auxiliary measurement (one JSON line, not the bench line): the chunk loop of an upsampling
     layer with the nearest-2x upsample fused into the conv, against the unfused pipeline that
@@ -947,6 +1010,8 @@ def main():
     ap.add_argument("--output-chunks", type=int, default=16)
     ap.add_argument("--graph-timing", action="store_true",
                     help="auxiliary: time the step eagerly and replayed from a CUDA graph")
+    ap.add_argument("--layer-group", action="store_true",
+                    help="auxiliary: time a frame-batched layer group of the decoder's last layers")
     ap.add_argument("--upsample-compare", action="store_true",
                     help="auxiliary: time an upsampling workload fused and with the upsample written to memory")
     args = ap.parse_args()
@@ -959,6 +1024,8 @@ def main():
         return run_single_chunk(args, wl)  # one 4-frame chunk: fits for every workload
     if args.output_path:
         return run_output_pipeline(args, wl)  # one 4-frame input chunk
+    if args.layer_group:
+        return run_layer_group(args, wl)
     if wl.T * wl.H * wl.W * max(wl.Cin, wl.Cout) * 2 > 32e9:
         log("%s does not fit resident on one device; it is covered by the streaming parity test" % wl.name)
         return 2

@@ -32,7 +32,8 @@ __all__ = [
     "library_path", "Upsample2xConvPlan",
     "load_library", "FrameWriter",
     "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
-    "weights_from_torch_layout", "EXPORTED_SYMBOLS",
+    "cc3d_group_create", "cc3d_group_workspace_bytes", "cc3d_group_forward_chunk", "cc3d_group_destroy",
+    "LayerGroup", "weights_from_torch_layout", "EXPORTED_SYMBOLS",
 ]
 
 CC3D_F32 = 0
@@ -50,6 +51,7 @@ EXPORTED_SYMBOLS = (
     "cc3d_status_string", "cc3d_plan_kernel", "cc3d_plan_launches_per_chunk", "cc3d_plan_describe",
     "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_debug_set_schedule", "cc3d_last_error_detail",
     "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
+    "cc3d_group_create", "cc3d_group_workspace_bytes", "cc3d_group_forward_chunk", "cc3d_group_destroy",
 )
 
 # the CC3D_SCHED_* knobs of cc3d.h, by name (value -1 restores the measured default)
@@ -112,6 +114,14 @@ def load_library():
         lib.cc3d_writer_close.argtypes = [vp, ctypes.POINTER(ctypes.c_longlong)]
         for f in (lib.cc3d_writer_create, lib.cc3d_writer_submit, lib.cc3d_writer_wait_copied,
                   lib.cc3d_writer_close):
+            f.restype = i
+        lib.cc3d_group_create.argtypes = [i, ctypes.POINTER(vp), i, ctypes.POINTER(vp)]
+        lib.cc3d_group_workspace_bytes.argtypes = [vp, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.cc3d_group_forward_chunk.argtypes = [vp, i, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                                 ctypes.POINTER(vp), vp, vp, ctypes.c_size_t, vp]
+        lib.cc3d_group_destroy.argtypes = [vp]
+        lib.cc3d_group_destroy.restype = None
+        for f in (lib.cc3d_group_create, lib.cc3d_group_workspace_bytes, lib.cc3d_group_forward_chunk):
             f.restype = i
         lib.cc3d_last_error_detail.argtypes = []
         lib.cc3d_last_error_detail.restype = ctypes.c_char_p
@@ -229,6 +239,41 @@ def cc3d_writer_close(writer) -> int:
     n = ctypes.c_longlong(0)
     _check(load_library().cc3d_writer_close(writer, ctypes.byref(n)), "cc3d_writer_close")
     return n.value
+
+
+def _ptr_array(items):
+    """A host array of device pointers (tensors, int addresses or None) for the group calls."""
+    if items is None:
+        return None
+    return (ctypes.c_void_p * len(items))(*[_addr(t) for t in items])
+
+
+def cc3d_group_create(plans, frame_batch: int):
+    """plans: C plan handles (or CausalConv3dPlan objects), first layer first."""
+    hs = [p.handle if hasattr(p, "handle") else p for p in plans]
+    arr = (ctypes.c_void_p * len(hs))(*hs)
+    g = ctypes.c_void_p()
+    _check(load_library().cc3d_group_create(len(hs), arr, int(frame_batch), ctypes.byref(g)), "cc3d_group_create")
+    return g.value
+
+
+def cc3d_group_workspace_bytes(group, T_max: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().cc3d_group_workspace_bytes(group, int(T_max), ctypes.byref(n)), "cc3d_group_workspace_bytes")
+    return n.value
+
+
+def cc3d_group_forward_chunk(group, T, x, w, b, cache_in, cache_out, y, workspace, workspace_bytes, stream=None):
+    """w, b, cache_in, cache_out: per-layer lists (b, cache_in may be None; entries may be None)."""
+    _check(load_library().cc3d_group_forward_chunk(group, int(T), _addr(x), _ptr_array(w), _ptr_array(b),
+                                                   _ptr_array(cache_in), _ptr_array(cache_out), _addr(y),
+                                                   _addr(workspace), int(workspace_bytes), _stream(stream)),
+           "cc3d_group_forward_chunk")
+
+
+def cc3d_group_destroy(group):
+    if group:
+        load_library().cc3d_group_destroy(group)
 
 
 class FrameWriter:
@@ -413,6 +458,60 @@ class CausalConv3dPlan:
     def close(self):
         if getattr(self, "handle", None):
             cc3d_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class LayerGroup:
+    """Consecutive layers (plans, first layer first) run frame batch by frame batch through the
+    C ABI's layer-group runtime: each batch of `frame_batch` frames (0: the whole chunk) passes
+    through every layer before the next batch starts, so only one batch of intermediate frames is
+    held; layers with a history keep it from batch to batch.  The plans must outlive the group."""
+
+    def __init__(self, plans, frame_batch: int = 1):
+        self.plans = list(plans)
+        self.frame_batch = int(frame_batch)
+        self.handle = cc3d_group_create(self.plans, self.frame_batch)
+
+    def workspace_bytes(self, T_max: int) -> int:
+        return cc3d_group_workspace_bytes(self.handle, T_max)
+
+    def new_workspace(self, T_max: int, device="cuda"):
+        """A workspace for chunks of up to T_max frames (allocated by PyTorch; 256-byte aligned)."""
+        import torch
+        n = self.workspace_bytes(T_max)
+        buf = torch.empty(n + 256, dtype=torch.uint8, device=device)
+        off = (-buf.data_ptr()) % 256
+        return buf[off:off + n]
+
+    def forward_chunk(self, x, ws, bs=None, caches_in=None, caches_out=None, y=None, workspace=None, stream=None):
+        """One chunk through the group; returns the last layer's output.  ws / bs / caches_in /
+        caches_out are per-layer lists (caches_in None: zero histories)."""
+        import torch
+        T = 0 if x is None else int(x.shape[0])
+        first, last = self.plans[0], self.plans[-1]
+        if y is None and T > 0:
+            y = torch.empty((T, last.Ho, last.Wo, last.Cout), dtype=last.torch_dtype(), device=x.device)
+        first._check_sizes(T, first.torch_dtype(), x=x)
+        last._check_sizes(T, last.torch_dtype(), y=y)
+        for j, p in enumerate(self.plans):
+            p._check_sizes(0, p.torch_dtype(), w=ws[j], b=None if bs is None else bs[j],
+                           cache_in=None if caches_in is None else caches_in[j],
+                           cache_out=None if caches_out is None else caches_out[j])
+        if workspace is None:
+            workspace = self.new_workspace(T, x.device if x is not None else "cuda")
+        nbytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+        cc3d_group_forward_chunk(self.handle, T, x, ws, bs, caches_in, caches_out, y, workspace, nbytes, stream)
+        return y
+
+    def close(self):
+        if getattr(self, "handle", None):
+            cc3d_group_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -531,6 +531,7 @@ cc3d_status cc3d_debug_set_schedule(cc3d_plan_t plan, int knob, int value)
 
 static size_t esize(const cc3d_plan_s* p) { return p->dtype == CC3D_F32 ? 4 : 2; }
 
+
 cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream)
 {
     if (plan == nullptr || cache == nullptr) return CC3D_ERR_INVALID_ARG;
@@ -573,9 +574,27 @@ cc3d_status cc3d_get_status(cc3d_plan_t plan, void* stream)
 
 }  // extern "C"
 
+bool cc3d::plan_shape(cc3d_plan_t plan, PlanShape* out)
+{
+    if (plan == nullptr || out == nullptr) return false;
+    out->Cin = plan->Cin;
+    out->Cout = plan->Cout;
+    out->H = plan->H;
+    out->W = plan->W;
+    out->Ho = plan->up2 ? 2 * plan->H : plan->H;
+    out->Wo = plan->up2 ? 2 * plan->W : plan->W;
+    out->kt = plan->kt;
+    out->kh = plan->kh;
+    out->kw = plan->kw;
+    out->esize = (int)esize(plan);
+    return true;
+}
+
 // Both forward entry points: y in the plan's dtype, or (out_u8, narrow-head plans) 8-bit pixels.
-static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b, const void* res,
-                                const void* cache_in, void* cache_out, void* y, void* stream_, bool out_u8)
+// With dry_run every check runs (arguments, device, configuration) and nothing is launched.
+cc3d_status cc3d::forward_impl(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b,
+                               const void* res, const void* cache_in, void* cache_out, void* y, void* stream_,
+                               bool out_u8, bool dry_run)
 {
     if (plan == nullptr || T < 0) return CC3D_ERR_INVALID_ARG;
     const cc3d_plan_s& p = *plan;
@@ -640,12 +659,13 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
 
     if (T == 0) {
         // only the history moves: cache_out = last P frames of cache_in (or zeros)
-        if (P == 0) return CC3D_OK;
+        if (P == 0 || dry_run) return CC3D_OK;
         const cudaError_t e = cache_update_launch(nullptr, cache_in, cache_out, 0, P, frame_in, stream);
         return e == cudaSuccess ? CC3D_OK : cuda_fail("cache update launch", e);
     }
 
     if (p.kind == K_SIMT_F32) {
+        if (dry_run) return CC3D_OK;
         SimtLaunch L;
         L.T = T;
         L.H = p.H;
@@ -668,15 +688,29 @@ static cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const vo
         return CC3D_OK;
     }
 
-    if (p.kind == K_TC_BF16_HEAD)
+    if (p.kind == K_TC_BF16_HEAD) {
+        if (dry_run) {
+            HeadLaunch hl;
+            memset(&hl, 0, sizeof(hl));
+            return head_configure(T, p.H, p.W, p.Cin, p.Cout, d->sms, &hl) ? CC3D_OK : CC3D_ERR_UNSUPPORTED;
+        }
         return head_forward(p, *d, T, x, w, b, res, cache_in, cache_out, y, stream, out_u8);
-    if (p.kind == K_TC_BF16_STREAM) return stream_forward(p, *d, T, x, w, b, res, cache_in, cache_out, y, stream);
+    }
+    if (p.kind == K_TC_BF16_STREAM) {
+        if (dry_run) {
+            StreamLaunch sl;
+            memset(&sl, 0, sizeof(sl));
+            return stream_configure(T, p.H, p.W, p.Cin, p.Cout, p.kt, d->sms, &sl) ? CC3D_OK : CC3D_ERR_UNSUPPORTED;
+        }
+        return stream_forward(p, *d, T, x, w, b, res, cache_in, cache_out, y, stream);
+    }
 
     // ---- tensor-core path
     TcLaunch L;
     memset(&L, 0, sizeof(L));
     if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, res != nullptr, p.up2 != 0, &p.ov, &L))
         return CC3D_ERR_UNSUPPORTED;
+    if (dry_run) return CC3D_OK;
     if (p.fault == 2) return cuda_fail("injected tensor-map encode failure");  // nothing launched
     const CUtensorMapSwizzle sw = p.CB == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : p.CB == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -798,13 +832,13 @@ extern "C" {
 cc3d_status cc3d_forward_chunk(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b,
                                const void* res, const void* cache_in, void* cache_out, void* y, void* stream)
 {
-    return forward_impl(plan, T, x, w, b, res, cache_in, cache_out, y, stream, false);
+    return forward_impl(plan, T, x, w, b, res, cache_in, cache_out, y, stream, false, false);
 }
 
 cc3d_status cc3d_forward_chunk_u8(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b,
                                   const void* res, const void* cache_in, void* cache_out, void* y_u8, void* stream)
 {
-    return forward_impl(plan, T, x, w, b, res, cache_in, cache_out, y_u8, stream, true);
+    return forward_impl(plan, T, x, w, b, res, cache_in, cache_out, y_u8, stream, true, false);
 }
 
 }  // extern "C"

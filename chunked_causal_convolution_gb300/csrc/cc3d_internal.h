@@ -173,4 +173,16 @@ cudaError_t cache_update_launch(const void* x, const void* cache_in, void* cache
                                 size_t frame_bytes, cudaStream_t stream);
 cudaError_t zero_fill_launch(void* p, size_t bytes, cudaStream_t stream);
 
+// One chunk of a plan (cc3d_forward_chunk, or cc3d_forward_chunk_u8 with out_u8).  With dry_run
+// every check of the call runs (arguments, device, launch configuration) and nothing is launched.
+cc3d_status forward_impl(cc3d_plan_t plan, int T, const void* x, const void* w, const void* b, const void* res,
+                         const void* cache_in, void* cache_out, void* y, void* stream, bool out_u8, bool dry_run);
+
+// A plan's shape, for the layer-group runtime (cc3d_group_*): input frames H x W x Cin, output
+// frames Ho x Wo x Cout, the kernel extent and the element size.
+struct PlanShape {
+    int Cin, Cout, H, W, Ho, Wo, kt, kh, kw, esize;
+};
+bool plan_shape(cc3d_plan_t plan, PlanShape* out);
+
 }  // namespace cc3d

@@ -195,6 +195,51 @@ cc3d_status cc3d_writer_submit(cc3d_writer_t w, const void* src, size_t bytes, v
 cc3d_status cc3d_writer_wait_copied(cc3d_writer_t w, long long seq, void* stream);
 cc3d_status cc3d_writer_close(cc3d_writer_t w, long long* bytes_written);
 
+/*
+ * Layer groups run frame batch by frame batch ("SwiftVR Inference Optimization"
+ * (LightX2V blog), section "ReAE Frame Batching": consecutive layers pass a small
+ * batch of frames through the whole group before the next batch starts, so only
+ * one batch's intermediate features exist at a time and the last layer writes into
+ * one output buffer; layers with a temporal history keep their state rules).
+ *
+ * cc3d_group_create: a group of nlayers (1..64) consecutive plans, run in order
+ *   on each batch of frame_batch frames (0: the whole chunk as one batch).  Layer
+ *   l + 1 reads what layer l writes: its input frames must be layer l's output
+ *   frames (channels and size; an upsampling plan doubles them) in the same dtype,
+ *   else CC3D_ERR_INVALID_ARG.  The host array is copied; the plans are not owned
+ *   and must outlive the group.
+ * cc3d_group_workspace_bytes: device bytes of workspace that a chunk of up to T_max
+ *   frames needs: two buffers that the intermediate batches alternate between
+ *   (each one batch of the largest layer output it holds), and, when a chunk takes
+ *   more than one batch, one more history buffer [kt-1][H][W][Cin] per layer with
+ *   a history.  0 for a one-layer group taking its chunk in one batch.
+ * cc3d_group_forward_chunk: one chunk of T_chunk frames through the group.
+ *   x_chunk   the first layer's input [T_chunk][H][W][Cin].
+ *   w, b      host arrays of nlayers device pointers (b, and any b[l], may be NULL).
+ *   cache_in  host array of nlayers history pointers, or NULL; an entry is NULL
+ *             for a zero history (and for kt = 1 layers).
+ *   cache_out host array of nlayers history buffers (entries of kt = 1 layers may
+ *             be NULL); each receives its layer's history after the chunk, as
+ *             cc3d_forward_chunk would leave it.
+ *   y         the last layer's output [T_chunk][Ho][Wo][Cout].
+ *   workspace device memory owned by the caller, 256-byte aligned, at least
+ *             cc3d_group_workspace_bytes(T_chunk) bytes (workspace_bytes gives its
+ *             size), overlapping nothing else; its contents need no initialisation
+ *             and are undefined afterwards.  May be NULL when 0 bytes are needed.
+ *   No residual inputs.  Every launch of the chunk is checked (as in
+ *   cc3d_forward_chunk) before the first one is enqueued; a failed check launches
+ *   nothing.  All work is enqueued on `stream`, in order.  The outputs and
+ *   histories equal those of running each layer's chunk loop over the whole chunk,
+ *   bit for bit.
+ */
+typedef struct cc3d_group_s* cc3d_group_t;
+cc3d_status cc3d_group_create(int nlayers, const cc3d_plan_t* plans, int frame_batch, cc3d_group_t* out);
+cc3d_status cc3d_group_workspace_bytes(cc3d_group_t g, int T_max, size_t* bytes);
+cc3d_status cc3d_group_forward_chunk(cc3d_group_t g, int T_chunk, const void* x_chunk, const void* const* w,
+                                     const void* const* b, const void* const* cache_in, void* const* cache_out,
+                                     void* y, void* workspace, size_t workspace_bytes, void* stream);
+void cc3d_group_destroy(cc3d_group_t g);
+
 /* Zero a cache buffer ([kt-1][H][W][Cin]) on the stream: the history of a new
  * video.  Stream-ordered, no allocation.  Same alignment rule as cache_out. */
 cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream);

@@ -414,3 +414,109 @@ def test_binding_refuses_a_tensor_of_another_device(monkeypatch):
         cc3d._addr(FakeCudaTensor())
     FakeCudaTensor.device = torch.device("cuda", 0)
     assert cc3d._addr(FakeCudaTensor()) == 0x10000
+
+
+def test_group_create_checks_the_layer_chain(lib):
+    a = cc3d.cc3d_plan_create(96, 64, 36, 64, 3, 3, 3, cc3d.CC3D_BF16)
+    b = cc3d.cc3d_plan_create(64, 32, 36, 64, 1, 1, 1, cc3d.CC3D_BF16)
+    c = cc3d.cc3d_plan_create(96, 32, 36, 64, 3, 3, 3, cc3d.CC3D_BF16)   # Cin does not follow a
+    d = cc3d.cc3d_plan_create(64, 32, 18, 32, 3, 3, 3, cc3d.CC3D_BF16)   # frame size does not follow a
+    u = cc3d.cc3d_plan_create_upsample2x(32, 16, 36, 64, 3, cc3d.CC3D_BF16)  # reads b's output, doubles it
+    v = cc3d.cc3d_plan_create(16, 3, 72, 128, 3, 3, 3, cc3d.CC3D_BF16)
+    try:
+        arr = lambda *ps: (ctypes.c_void_p * len(ps))(*ps)  # noqa: E731
+        g = ctypes.c_void_p(1)
+        assert lib.cc3d_group_create(0, arr(a), 1, ctypes.byref(g)) == 1 and g.value is None
+        assert lib.cc3d_group_create(1, arr(a), -1, ctypes.byref(g)) == 1
+        assert lib.cc3d_group_create(2, arr(a, c), 1, ctypes.byref(g)) == 1
+        assert lib.cc3d_group_create(2, arr(a, d), 1, ctypes.byref(g)) == 1
+        assert lib.cc3d_group_create(2, arr(a, None), 1, ctypes.byref(g)) == 1
+        h = cc3d.cc3d_group_create([a, b, u, v], 2)
+        cc3d.cc3d_group_destroy(h)
+    finally:
+        for p in (a, b, c, d, u, v):
+            cc3d.cc3d_destroy(p)
+
+
+def test_group_workspace_sizes(lib):
+    """Two buffers for the intermediate batches (each one batch of the largest output it holds),
+    plus one more history per causal layer when a chunk takes several batches; 256-byte sections."""
+    H, W = 360, 640
+    px = H * W
+    a = cc3d.cc3d_plan_create(96, 96, H, W, 3, 3, 3, cc3d.CC3D_BF16)
+    b = cc3d.cc3d_plan_create(96, 192, H, W, 1, 1, 1, cc3d.CC3D_BF16)
+    c = cc3d.cc3d_plan_create(192, 3, H, W, 3, 3, 3, cc3d.CC3D_BF16)
+    try:
+        g1 = cc3d.cc3d_group_create([a, b, c], 1)
+        g0 = cc3d.cc3d_group_create([a, b, c], 0)
+        gs = cc3d.cc3d_group_create([a], 1)
+        # frame batch 1, 4-frame chunks: buffer 0 holds a's 96-channel frame, buffer 1 b's
+        # 192-channel frame; histories of a (2 x 96 channels) and c (2 x 192 channels)
+        exp1 = px * 96 * 2 + px * 192 * 2 + 2 * px * 96 * 2 + 2 * px * 192 * 2
+        assert cc3d.cc3d_group_workspace_bytes(g1, 4) == exp1
+        assert cc3d.cc3d_group_workspace_bytes(g1, 1) == px * 96 * 2 + px * 192 * 2  # one batch: no extra history
+        # whole chunk: both intermediates of all 4 frames, no extra history
+        assert cc3d.cc3d_group_workspace_bytes(g0, 4) == 4 * (px * 96 * 2 + px * 192 * 2)
+        assert cc3d.cc3d_group_workspace_bytes(g0, 0) == 0
+        # a single layer needs only its second history
+        assert cc3d.cc3d_group_workspace_bytes(gs, 4) == 2 * px * 96 * 2
+        assert cc3d.cc3d_group_workspace_bytes(gs, 1) == 0
+        # odd sizes are rounded up to 256-byte sections
+        o1 = cc3d.cc3d_plan_create(16, 16, 3, 5, 1, 1, 1, cc3d.CC3D_BF16)
+        o2 = cc3d.cc3d_plan_create(16, 16, 3, 5, 1, 1, 1, cc3d.CC3D_BF16)
+        go = cc3d.cc3d_group_create([o1, o2], 1)
+        assert cc3d.cc3d_group_workspace_bytes(go, 3) == 512  # 15 * 16 * 2 = 480 -> 512
+        for h in (g1, g0, gs, go):
+            cc3d.cc3d_group_destroy(h)
+        for p in (o1, o2):
+            cc3d.cc3d_destroy(p)
+    finally:
+        for p in (a, b, c):
+            cc3d.cc3d_destroy(p)
+
+
+def test_group_forward_rejects_before_any_device_work(lib):
+    a = cc3d.cc3d_plan_create(32, 32, 4, 8, 3, 3, 3, cc3d.CC3D_BF16)
+    b = cc3d.cc3d_plan_create(32, 16, 4, 8, 1, 1, 1, cc3d.CC3D_BF16)
+    g = cc3d.cc3d_group_create([a, b], 1)
+    try:
+        need = cc3d.cc3d_group_workspace_bytes(g, 2)
+        buf = (ctypes.c_uint8 * (1 << 20))()
+        base = (ctypes.addressof(buf) + 255) & ~255
+        x, y, w0, w1, c0, c1, ws = (base, base + 8192, base + 16384, base + 81920, base + 98304, base + 106496,
+                                    base + 131072)
+        W = (ctypes.c_void_p * 2)(w0, w1)
+        CO = (ctypes.c_void_p * 2)(c1, None)
+        f = lib.cc3d_group_forward_chunk
+        assert f(None, 2, x, W, None, None, CO, y, ws, need, None) == 1          # null group
+        assert f(g, -1, x, W, None, None, CO, y, ws, need, None) == 1            # negative T
+        assert f(g, 2, x, None, None, None, CO, y, ws, need, None) == 1          # no weights
+        assert f(g, 2, x, W, None, None, None, y, ws, need, None) == 1           # no histories
+        assert f(g, 2, x, W, None, None, CO, y, ws, need - 1, None) == 1         # workspace too small
+        assert f(g, 2, x, W, None, None, CO, y, None, need, None) == 1           # no workspace
+        assert f(g, 2, x, W, None, None, CO, y, ws + 16, need, None) == 3        # workspace misaligned
+        assert f(g, 2, x, W, None, None, CO, y, x, need, None) == 4              # workspace over x
+        assert f(g, 2, x, W, None, None, CO, y, w0, need, None) == 4             # workspace over a weight
+        # host memory: refused by the check of the first launch, nothing launched
+        assert f(g, 2, x, W, None, None, CO, y, ws, need, None) == 8
+    finally:
+        cc3d.cc3d_group_destroy(g)
+        cc3d.cc3d_destroy(a)
+        cc3d.cc3d_destroy(b)
+
+
+def test_frame_batching_holds_one_batch_of_intermediates(lib):
+    """The decoder tail at the c96 stage (two 96-channel 3x3x3 convs and the 3-channel head) on the
+    pages' 24-frame chunks: batches of one frame hold two intermediate frames and one more history
+    per layer, the whole chunk at once holds both 24-frame intermediates."""
+    H, W = 360, 640
+    plans = [cc3d.CausalConv3dPlan(96, 96, H, W), cc3d.CausalConv3dPlan(96, 96, H, W),
+             cc3d.CausalConv3dPlan(96, 3, H, W)]
+    frame = H * W * 96 * 2
+    whole = cc3d.LayerGroup(plans, 0).workspace_bytes(24)
+    one = cc3d.LayerGroup(plans, 1).workspace_bytes(24)
+    two = cc3d.LayerGroup(plans, 2).workspace_bytes(24)
+    assert whole == 2 * 24 * frame
+    assert one == 2 * frame + 3 * 2 * frame
+    assert two == 2 * 2 * frame + 3 * 2 * frame
+    assert whole / one == 6.0

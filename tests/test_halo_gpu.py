@@ -1,7 +1,8 @@
 """The time-split runner with the library's layers on one GPU (a single rank: the exchange is
 the hand-over of each layer's history from one wave to the next): a stack of layers run wave by
 wave through halo.TimeSplit equals the plain chunk loop over the whole video bit for bit (the
-library's result does not depend on where the video is cut), and the oracle within tolerance."""
+library's result does not depend on where the video is cut), and each layer of that loop is within
+tolerance of the oracle on the bf16 input it read."""
 import numpy as np
 import pytest
 import torch
@@ -38,16 +39,19 @@ def test_waves_through_the_time_split_equal_the_chunk_loop():
     ys = [split.forward(x[a:b]) for a, b in ((0, 5), (5, 6), (6, 11))]
     y_split = torch.cat(ys)
     # the same stack, each layer as one chunk loop over the whole video
-    cur = x
+    cur, outs = x, []
     for plan, (w, b, _) in zip(plans, params):
         cur, _ = run_chunks(plan, cur, w, b, None, [4, 4, 3])
+        outs.append(cur)
     assert all(p.status() == 0 for p in plans)
     assert torch.equal(y_split, cur)
-    ref = to_f64(raw["x"], "bf16")
-    for (w, b, p), plan in zip(params, plans):
-        ref = oracle.conv_whole(ref, to_f64(p["w"], "bf16"), to_f64(p["b"], "bf16"))
-        ref = oracle.round_bf16(ref)  # the next layer reads the bf16 values this layer stored
-    err = np.abs(from_device(y_split) - ref).max()
-    assert err <= tolerance("bf16", ref), err
+    # every layer against the oracle on the bf16 input it read (the previous layer's stored output)
+    inp = to_f64(raw["x"], "bf16")
+    for j, (w, b, p) in enumerate(params):
+        ref = oracle.conv_whole(inp, to_f64(p["w"], "bf16"), to_f64(p["b"], "bf16"))
+        got = from_device(outs[j])
+        err = np.abs(got - ref).max()
+        assert err <= tolerance("bf16", ref), (j, err)
+        inp = got
     for plan in plans:
         plan.close()

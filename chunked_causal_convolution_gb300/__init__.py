@@ -42,7 +42,7 @@ CC3D_BF16 = 1
 STATUS_NAMES = {
     0: "CC3D_OK", 1: "CC3D_ERR_INVALID_ARG", 2: "CC3D_ERR_UNSUPPORTED", 3: "CC3D_ERR_ALIGNMENT",
     4: "CC3D_ERR_ALIAS", 5: "CC3D_ERR_CUDA", 6: "CC3D_ERR_OOM", 7: "CC3D_ERR_DEVICE_TIMEOUT",
-    8: "CC3D_ERR_NOT_DEVICE_MEMORY", 9: "CC3D_ERR_IO",
+    8: "CC3D_ERR_NOT_DEVICE_MEMORY", 9: "CC3D_ERR_IO", 10: "CC3D_ERR_SCRATCH_TOO_SMALL",
 }
 
 EXPORTED_SYMBOLS = (
@@ -52,6 +52,7 @@ EXPORTED_SYMBOLS = (
     "cc3d_debug_set_wait_budget_ns", "cc3d_debug_set_fault", "cc3d_debug_set_schedule", "cc3d_last_error_detail",
     "cc3d_writer_create", "cc3d_writer_submit", "cc3d_writer_wait_copied", "cc3d_writer_close",
     "cc3d_group_create", "cc3d_group_workspace_bytes", "cc3d_group_forward_chunk", "cc3d_group_destroy",
+    "cc3d_group_forward_chunk_static",
 )
 
 # the CC3D_SCHED_* knobs of cc3d.h, by name (value -1 restores the measured default)
@@ -119,6 +120,9 @@ def load_library():
         lib.cc3d_group_workspace_bytes.argtypes = [vp, i, ctypes.POINTER(ctypes.c_size_t)]
         lib.cc3d_group_forward_chunk.argtypes = [vp, i, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                                  ctypes.POINTER(vp), vp, vp, ctypes.c_size_t, vp]
+        lib.cc3d_group_forward_chunk_static.argtypes = [vp, i, vp, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                                        ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp]
+        lib.cc3d_group_forward_chunk_static.restype = i
         lib.cc3d_group_destroy.argtypes = [vp]
         lib.cc3d_group_destroy.restype = None
         for f in (lib.cc3d_group_create, lib.cc3d_group_workspace_bytes, lib.cc3d_group_forward_chunk):
@@ -269,6 +273,15 @@ def cc3d_group_forward_chunk(group, T, x, w, b, cache_in, cache_out, y, workspac
                                                    _ptr_array(cache_in), _ptr_array(cache_out), _addr(y),
                                                    _addr(workspace), int(workspace_bytes), _stream(stream)),
            "cc3d_group_forward_chunk")
+
+
+def cc3d_group_forward_chunk_static(group, T, x, w, b, cache_in, cache_out, y, stream=None):
+    """cc3d_group_forward_chunk with the library's fixed device scratch array as its workspace:
+    allocates nothing, for callers that cannot allocate device memory (see include/cc3d.h)."""
+    _check(load_library().cc3d_group_forward_chunk_static(group, int(T), _addr(x), _ptr_array(w), _ptr_array(b),
+                                                          _ptr_array(cache_in), _ptr_array(cache_out), _addr(y),
+                                                          _stream(stream)),
+           "cc3d_group_forward_chunk_static")
 
 
 def cc3d_group_destroy(group):

@@ -328,6 +328,7 @@ const char* cc3d_status_string(cc3d_status s)
     case CC3D_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
     case CC3D_ERR_NOT_DEVICE_MEMORY: return "pointer is not device memory";
     case CC3D_ERR_IO: return "host file could not be opened or written";
+    case CC3D_ERR_SCRATCH_TOO_SMALL: return "the call needs more than the library's fixed device scratch array";
     }
     return "unknown status";
 }

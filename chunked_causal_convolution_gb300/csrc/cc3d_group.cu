@@ -14,6 +14,7 @@
 // chunk loop bit for bit.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -21,6 +22,13 @@
 #include "cc3d_internal.h"
 
 using namespace cc3d;
+
+// Workspace for cc3d_group_forward_chunk_static: a fixed array in device memory that exists on
+// every GPU where this library's device code is loaded, so that callers who cannot allocate device
+// memory still get frame batching.  In host code the name is only a stand-in, not a device
+// address: static_scratch() below looks the address up once per device, with that device current.
+static constexpr size_t kStaticScratchBytes = CC3D_GROUP_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_group_scratch[kStaticScratchBytes];
 
 struct cc3d_group_s {
     std::vector<cc3d_plan_t> plans;
@@ -87,6 +95,31 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb)
     if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
     const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
     return pa < pb + nb && pb < pa + na;
+}
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxScratchDevices] = {};
+
+// The device address of g_group_scratch on the current device (looked up on the first call there).
+cc3d_status static_scratch(void** out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) {
+        cudaGetLastError();
+        return CC3D_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_group_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return CC3D_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return CC3D_OK;
 }
 
 }  // namespace
@@ -202,6 +235,22 @@ cc3d_status cc3d_group_forward_chunk(cc3d_group_t g, int T, const void* x, const
         }
     }
     return CC3D_OK;
+}
+
+cc3d_status cc3d_group_forward_chunk_static(cc3d_group_t g, int T, const void* x, const void* const* w,
+                                            const void* const* b, const void* const* cache_in, void* const* cache_out,
+                                            void* y, void* stream)
+{
+    if (g == nullptr || T < 0) return CC3D_ERR_INVALID_ARG;
+    // the first call on a device looks up the array's address there
+    void* scratch = nullptr;
+    const cc3d_status st = static_scratch(&scratch);
+    if (st != CC3D_OK) return st;
+    // nothing in the array has to start at zero: every intermediate batch and history the chunk
+    // reads from it is written earlier in the same chunk, so the previous call's contents never
+    // matter
+    if (layout(*g, T).bytes > kStaticScratchBytes) return CC3D_ERR_SCRATCH_TOO_SMALL;
+    return cc3d_group_forward_chunk(g, T, x, w, b, cache_in, cache_out, y, scratch, kStaticScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -81,7 +81,9 @@ typedef enum {
     CC3D_ERR_OOM = 6,             /* host allocation failed                         */
     CC3D_ERR_DEVICE_TIMEOUT = 7,  /* a bounded wait inside a kernel ran out          */
     CC3D_ERR_NOT_DEVICE_MEMORY = 8, /* a tensor pointer is not device-accessible      */
-    CC3D_ERR_IO = 9                /* a host file could not be opened or written      */
+    CC3D_ERR_IO = 9,               /* a host file could not be opened or written      */
+    CC3D_ERR_SCRATCH_TOO_SMALL = 10 /* the call needs more than the library's fixed
+                                       device scratch array holds                   */
 } cc3d_status;
 
 /*
@@ -239,6 +241,39 @@ cc3d_status cc3d_group_forward_chunk(cc3d_group_t g, int T_chunk, const void* x_
                                      const void* const* b, const void* const* cache_in, void* const* cache_out,
                                      void* y, void* workspace, size_t workspace_bytes, void* stream);
 void cc3d_group_destroy(cc3d_group_t g);
+
+/*
+ * cc3d_group_forward_chunk without a caller-provided workspace; it allocates
+ * nothing.  (The pages have no counterpart of this call: it is an addition for
+ * callers that cannot allocate device memory themselves -- for example a plugin
+ * running inside a host framework whose allocator owns the GPU's memory and hands
+ * the plugin only its input and output buffers, or a processing loop that must
+ * not allocate once it is running, since cudaMalloc and cudaFree can synchronise
+ * the device and take an unbounded time.)
+ *
+ * The workspace is instead a fixed array of CC3D_GROUP_STATIC_SCRATCH_BYTES
+ * (64 MiB) in device memory, declared in the library itself: every GPU on which
+ * the library's device code is loaded holds it until the process exits.  A chunk
+ * whose workspace (cc3d_group_workspace_bytes(g, T_chunk)) exceeds it is refused
+ * with CC3D_ERR_SCRATCH_TOO_SMALL before anything is launched; use
+ * cc3d_group_forward_chunk with your own workspace for such groups.  The caller
+ * still provides the inputs, outputs and histories, exactly as for
+ * cc3d_group_forward_chunk (same arguments without the workspace, same checks,
+ * same results).
+ *
+ * The first call on each device looks up the array's device address there (one
+ * CUDA runtime query with that device current; later calls reuse it), so make
+ * the first call on a device before any stream capture on it.  The array keeps
+ * whatever the last call left in it; nothing in it needs to start at zero, as a
+ * chunk writes every part of it that it reads.  All calls on one device share
+ * the one array: two calls whose work overlaps on the GPU (e.g. on two streams
+ * without an event between them) race and corrupt each other's intermediates;
+ * order them on one stream or with events.
+ */
+#define CC3D_GROUP_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
+cc3d_status cc3d_group_forward_chunk_static(cc3d_group_t g, int T_chunk, const void* x_chunk, const void* const* w,
+                                            const void* const* b, const void* const* cache_in,
+                                            void* const* cache_out, void* y, void* stream);
 
 /* Zero a cache buffer ([kt-1][H][W][Cin]) on the stream: the history of a new
  * video.  Stream-ordered, no allocation.  Same alignment rule as cache_out. */

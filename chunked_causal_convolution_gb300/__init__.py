@@ -58,7 +58,7 @@ EXPORTED_SYMBOLS = (
 # the CC3D_SCHED_* knobs of cc3d.h, by name (value -1 restores the measured default)
 SCHEDULE_KNOBS = {
     "pair": 0, "two_frame": 1, "split_tail": 2, "channel_blocks": 3, "mma_warps": 4, "row_groups": 5,
-    "acc_stages": 6, "tap_rows": 7, "window_stages": 8, "weight_stages": 9, "prefetch": 10,
+    "acc_stages": 6, "tap_rows": 7, "window_stages": 8, "weight_stages": 9, "prefetch": 10, "channel_block": 11,
 }
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

@@ -313,6 +313,17 @@ static cc3d_status stream_forward(const cc3d_plan_s& p, const DeviceInfo& d, int
     return e == cudaSuccess ? CC3D_OK : cuda_fail("streaming kernel launch", e);
 }
 
+// The plan's input-channel block (the K step of the tensor-core kernels), 16 or 32 channels; the
+// CC3D_SCHED_CHANNEL_BLOCK knob may choose 16 for a plan whose Cin allows 32 (it changes the order
+// in which the products of every output are summed, the same way for every chunk of the plan).
+static int plan_cb(const cc3d_plan_s& p)
+{
+    const int v = p.ov.get(CC3D_SCHED_CHANNEL_BLOCK, 0);
+    if (v == 16 && p.Cin % 16 == 0) return 16;
+    if (v == 32 && p.Cin % 32 == 0) return 32;
+    return p.CB;
+}
+
 extern "C" {
 
 const char* cc3d_status_string(cc3d_status s)
@@ -478,7 +489,8 @@ cc3d_status cc3d_plan_describe(cc3d_plan_t plan, int T, int has_residual, char* 
     } else {
         TcLaunch L;
         memset(&L, 0, sizeof(L));
-        if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, has_residual != 0, p.up2 != 0, &p.ov, &L))
+        if (!tc_configure(plan_cb(p), T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, has_residual != 0, p.up2 != 0, &p.ov,
+                          &L))
             return CC3D_ERR_UNSUPPORTED;
         const int tiles = L.g.tiles_per_cb * L.g.ncolblk * (L.tstack ? (T + 1) / 2 : T) * L.ncoblk;
         // history frames the forward call hands to a copy engine (when the side stream is available)
@@ -489,7 +501,7 @@ cc3d_status cc3d_plan_describe(cc3d_plan_t plan, int T, int has_residual, char* 
                      "window_stages=%d weight_stages=%d window_stage_bytes=%d weight_stage_bytes=%d acc_stages=%d "
                      "mma_warps=%d split_n=%d tmem_cols=%d smem_bytes=%zu tiles=%d history_frames_on_copy_engine=%d",
                      L.tstack ? "tc2s_bf16_kernel" : (L.pair ? "tc2_bf16_kernel" : "tc_bf16_kernel"), L.pair,
-                     L.tstack, L.up2, p.CB, L.NT, L.nsplit, L.ncoblk, L.g.sub, L.g.S, L.g.row_aligned, L.g.nrows,
+                     L.tstack, L.up2, plan_cb(p), L.NT, L.nsplit, L.ncoblk, L.g.sub, L.g.S, L.g.row_aligned, L.g.nrows,
                      L.rb, L.na, L.nb, L.a_stage_bytes, L.b_stage_bytes, L.acc_stages, L.issuers, L.split_n,
                      L.tmem_cols, L.smem_bytes, tiles, n_ce);
     }
@@ -519,18 +531,20 @@ cc3d_status cc3d_debug_set_schedule(cc3d_plan_t plan, int knob, int value)
     // [lo, hi] of every knob; value -1 restores the measured default
     static const int range[CC3D_SCHED_COUNT][2] = {
         {0, 1}, {0, 1}, {0, 1}, {0, 1}, {1, 2}, {1, 4}, {1, kMaxAccStages}, {1, 3}, {2, kMaxRingStages},
-        {2, kMaxRingStages}, {0, 3}};
+        {2, kMaxRingStages}, {0, 3}, {16, 32}};
     if (plan == nullptr || knob < 0 || knob >= CC3D_SCHED_COUNT) return CC3D_ERR_INVALID_ARG;
     if (value != -1) {
         if (value < range[knob][0] || value > range[knob][1]) return CC3D_ERR_INVALID_ARG;
         if (knob == CC3D_SCHED_ROW_GROUPS && value == 3) return CC3D_ERR_INVALID_ARG;
         if (knob == CC3D_SCHED_TAP_ROWS && value == 2) return CC3D_ERR_INVALID_ARG;
+        if (knob == CC3D_SCHED_CHANNEL_BLOCK && value != 16 && value != 32) return CC3D_ERR_INVALID_ARG;
     }
     plan->ov.v[knob] = value;
     return CC3D_OK;
 }
 
 static size_t esize(const cc3d_plan_s* p) { return p->dtype == CC3D_F32 ? 4 : 2; }
+
 
 
 cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream)
@@ -709,19 +723,20 @@ cc3d_status cc3d::forward_impl(cc3d_plan_t plan, int T, const void* x, const voi
     // ---- tensor-core path
     TcLaunch L;
     memset(&L, 0, sizeof(L));
-    if (!tc_configure(p.CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, res != nullptr, p.up2 != 0, &p.ov, &L))
+    const int CB = plan_cb(p);
+    if (!tc_configure(CB, T, p.H, p.W, p.Cin, p.Cout, p.kt, p.kh, res != nullptr, p.up2 != 0, &p.ov, &L))
         return CC3D_ERR_UNSUPPORTED;
     if (dry_run) return CC3D_OK;
     if (p.fault == 2) return cuda_fail("injected tensor-map encode failure");  // nothing launched
-    const CUtensorMapSwizzle sw = p.CB == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : p.CB == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+    const CUtensorMapSwizzle sw = CB == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : CB == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                : CU_TENSOR_MAP_SWIZZLE_32B;
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     {
         const cuuint64_t dims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)T};
         const cuuint64_t strides[3] = {(cuuint64_t)p.Cin * 2, (cuuint64_t)p.W * p.Cin * 2,
                                        (cuuint64_t)p.H * p.W * p.Cin * 2};
-        const cuuint32_t box[4] = {(cuuint32_t)p.CB, (cuuint32_t)L.g.Sp, (cuuint32_t)L.g.nrows, 1};
+        const cuuint32_t box[4] = {(cuuint32_t)CB, (cuuint32_t)L.g.Sp, (cuuint32_t)L.g.nrows, 1};
         if (g_encode(&L.map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -739,7 +754,7 @@ cc3d_status cc3d::forward_impl(cc3d_plan_t plan, int T, const void* x, const voi
         const int taps = p.kt * p.kh * p.kw;
         const cuuint64_t dims[3] = {(cuuint64_t)p.Cin, (cuuint64_t)p.Cout, (cuuint64_t)taps};
         const cuuint64_t strides[2] = {(cuuint64_t)taps * p.Cin * 2, (cuuint64_t)p.Cin * 2};
-        const cuuint32_t box[3] = {(cuuint32_t)p.CB, (cuuint32_t)(L.pair ? L.NT / 2 : L.NT),
+        const cuuint32_t box[3] = {(cuuint32_t)CB, (cuuint32_t)(L.pair ? L.NT / 2 : L.NT),
                                    (cuuint32_t)(p.kh * L.rb)};
         if (g_encode(&L.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -747,7 +762,7 @@ cc3d_status cc3d::forward_impl(cc3d_plan_t plan, int T, const void* x, const voi
             return cuda_fail("cuTensorMapEncodeTiled (w)");
         if (L.tstack) {
             // the two-frame schedule's stacked stages: all NT rows of rb tap rows per block
-            const cuuint32_t box2[3] = {(cuuint32_t)p.CB, (cuuint32_t)L.NT, (cuuint32_t)(p.kh * L.rb)};
+            const cuuint32_t box2[3] = {(cuuint32_t)CB, (cuuint32_t)L.NT, (cuuint32_t)(p.kh * L.rb)};
             if (g_encode(&L.map_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box2,
                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -820,7 +835,7 @@ cc3d_status cc3d::forward_impl(cc3d_plan_t plan, int T, const void* x, const voi
         }
         if (e != cudaSuccess) return cuda_fail("history copy on the side streams", e);
     }
-    cudaError_t e = tc_launch(p.CB, L, stream);
+    cudaError_t e = tc_launch(CB, L, stream);
     if (e != cudaSuccess) return cuda_fail("tensor-core kernel launch", e);
     for (int i = 0; side_copy && i < cc3d_plan_s::kSide; ++i)
         if ((e = cudaStreamWaitEvent(stream, plan->join[i], 0)) != cudaSuccess)

@@ -340,9 +340,9 @@ cc3d_status cc3d_debug_set_fault(cc3d_plan_t plan, int mode);
  * Schedule overrides of the bf16 tensor-core families "tc_bf16", "tc_bf16_pair",
  * "tc_bf16_narrow" and "tc_bf16_up2" (for tuning sweeps and for the tests that
  * compare two schedules bit for bit; never needed in normal use).  Every knob
- * starts at -1, the measured default for the chunk's shape.  A knob changes only
- * how the work is tiled: the accumulation order of every output is fixed, so
- * every schedule gives the same bits.  A combination with no configuration makes
+ * starts at -1, the measured default for the chunk's shape.  A knob other than
+ * CC3D_SCHED_CHANNEL_BLOCK changes only how the work is tiled: the accumulation
+ * order of every output is fixed, so every schedule gives the same bits.  A combination with no configuration makes
  * cc3d_forward_chunk return CC3D_ERR_UNSUPPORTED (nothing launched); one whose
  * shared memory does not fit the SM is refused by the launch (CC3D_ERR_CUDA).
  * The plan's settings are its own: nothing is read from the environment.
@@ -362,7 +362,11 @@ typedef enum {
     CC3D_SCHED_WINDOW_STAGES = 8,  /* 2..8: input-window ring depth */
     CC3D_SCHED_WEIGHT_STAGES = 9,  /* 2..8: upper bound of the weight ring depth */
     CC3D_SCHED_PREFETCH = 10,      /* 0..3: temporal taps of the next tile warmed in L2 */
-    CC3D_SCHED_COUNT = 11
+    CC3D_SCHED_CHANNEL_BLOCK = 11, /* 16 or 32: input channels per K block (where Cin allows).  Unlike
+                                      the other knobs it changes the order in which each output's
+                                      products are summed (so the low bits of the result), the same
+                                      way for every chunk: set it before a video's first chunk */
+    CC3D_SCHED_COUNT = 12
 } cc3d_schedule_knob;
 cc3d_status cc3d_debug_set_schedule(cc3d_plan_t plan, int knob, int value);
 

@@ -351,10 +351,15 @@ def test_schedule_knobs_are_validated_and_plan_local(lib):
     try:
         f = lib.cc3d_debug_set_schedule
         assert f(None, 0, 1) == 1                              # null plan
-        assert f(p, -1, 0) == 1 and f(p, 11, 0) == 1           # unknown knobs
-        for knob, bad in ((0, 2), (1, -2), (4, 3), (5, 3), (5, 8), (6, 3), (7, 2), (8, 1), (9, 9), (10, 4)):
+        assert f(p, -1, 0) == 1 and f(p, 12, 0) == 1           # unknown knobs
+        for knob, bad in ((0, 2), (1, -2), (4, 3), (5, 3), (5, 8), (6, 3), (7, 2), (8, 1), (9, 9), (10, 4), (11, 24),
+                          (11, 64)):
             assert f(p, knob, bad) == 1, (knob, bad)
         assert cc3d.cc3d_plan_describe(p, 4)["kernel"] == "tc2s_bf16_kernel"
+        cc3d.cc3d_debug_set_schedule(p, "channel_block", 16)
+        assert cc3d.cc3d_plan_describe(p, 4)["channel_block"] == 16
+        cc3d.cc3d_debug_set_schedule(p, "channel_block", -1)
+        assert cc3d.cc3d_plan_describe(p, 4)["channel_block"] == 32
         cc3d.cc3d_debug_set_schedule(p, "two_frame", 0)
         assert cc3d.cc3d_plan_describe(p, 4)["kernel"] == "tc2_bf16_kernel"
         cc3d.cc3d_debug_set_schedule(p, "pair", 0)

@@ -201,7 +201,7 @@ bool side_stream_ready(cc3d_plan_s* p)
 }  // namespace
 
 // Narrow-output launch: tensor maps with one-row boxes for the staged input rows (loads) and the
-// new history (stores), and a (32 channels, Cout, 9 taps) box for the weights of one (dt,
+// new history (stores, from staged row 8 on), and a (32 channels, Cout, 9 taps) box for the weights of one (dt,
 // channel block).
 static cc3d_status head_forward(const cc3d_plan_s& p, const DeviceInfo& d, int T, const void* x, const void* w,
                                 const void* b, const void* res, const void* cache_in, void* cache_out, void* y,
@@ -214,7 +214,7 @@ static cc3d_status head_forward(const cc3d_plan_s& p, const DeviceInfo& d, int T
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const cuuint64_t strides[3] = {(cuuint64_t)p.Cin * 2, (cuuint64_t)p.W * p.Cin * 2,
                                    (cuuint64_t)p.H * p.W * p.Cin * 2};
-    const cuuint32_t box[4] = {32, 136, 1, 1};
+    const cuuint32_t box[4] = {32, 128, 1, 1};  // the 128 input positions of a strip
     const cuuint64_t dims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)T};
     if (g_encode(&L.map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -229,7 +229,7 @@ static cc3d_status head_forward(const cc3d_plan_s& p, const DeviceInfo& d, int T
     }
     {
         const cuuint64_t cdims[4] = {(cuuint64_t)p.Cin, (cuuint64_t)p.W, (cuuint64_t)p.H, 2};
-        const cuuint32_t sbox[4] = {32, 126, 1, 1};
+        const cuuint32_t sbox[4] = {32, 120, 1, 1};  // staged rows 8 .. 127 (positions w0 + 7 .. w0 + 126)
         if (g_encode(&L.map_cache_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache_out, cdims, strides, sbox, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)

@@ -12,8 +12,10 @@
 // and neighbouring rows (running sums kept in registers).  A block walks a contiguous run of rows
 // of one column strip (126 output pixels = 128 input positions with the halo), input row by input
 // row; every input row (all channels, the chunk's frames and the two history frames) is loaded
-// into shared memory once, and TMA stores write the new history (the last two input frames)
-// back from there.  Rows are dealt out to the blocks in equal runs, so there is no tail wave.
+// into shared memory once -- exactly the 128 positions the MMA reads -- and the new history (the
+// last two input frames) is written back from there (TMA stores from a swizzle-atom boundary on,
+// a warp copy for the strip's first pixels).  Rows are dealt out to the blocks in equal runs, so
+// there is no tail wave.
 //
 // Accumulation order of one output (t, h, w, co), fixed whatever the chunking: inside the tensor
 // core dt, channel block, 16-channel step; then ((dh = 0) + (dh = 1)) + (dh = 2), each dh term
@@ -35,8 +37,13 @@ constexpr int kHeadMaxStages = 8;        // input-row stages
 constexpr int kHeadSlots = 2;            // input rows whose sums sit in tensor memory at once
 constexpr int kHeadPos = 128;            // input positions per strip (the MMA's M)
 constexpr int kHeadOut = kHeadPos - 2;   // output pixels per strip
-constexpr int kHeadLead = 8;             // staged positions before the strip's first output pixel
-constexpr int kHeadBox = 136;            // staged positions: w0 - 8 .. w0 + 127 (MMA rows 7 .. 134)
+constexpr int kHeadLead = 1;             // staged positions before the strip's first output pixel
+constexpr int kHeadBox = 128;            // staged positions: w0 - 1 .. w0 + 126 (the MMA's rows)
+// the history of staged rows kHeadStoreRow .. kHeadBox - 1 (positions w0 + 7 .. w0 + 126) is stored
+// by TMA, whose shared-memory source must start on a 512-byte swizzle atom (row 8); a warp copies
+// rows 1 .. 7 (positions w0 .. w0 + 6).  Position w0 + 126 is the next strip's first pixel: both
+// strips write the same bytes there.
+constexpr int kHeadStoreRow = 8;
 constexpr int kHeadEdge = 16;            // floats per (frame, warp, side) in the edge exchange
 
 template <int COUT>
@@ -107,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
     extern __shared__ uint8_t dsm_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* smW = sm;                                 // [dt][channel block] tiles of NCOL rows x 64 B
-    uint8_t* smX = sm + (size_t)L.w_bytes;             // stages of [channel block][136 positions] x 64 B
+    uint8_t* smX = sm + (size_t)L.w_bytes;             // stages of [channel block][128 positions] x 64 B
     float* s_edge = reinterpret_cast<float*>(smX + (size_t)L.nstages * L.x_stage_bytes);  // [2][EBUF]
 
     __shared__ uint64_t x_full[kHeadMaxStages], x_empty[kHeadMaxStages], w_full, acc_full[kHeadSlots],
@@ -287,10 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
     } else if (warp == 3) {
         // ------------------------------------------------------------ temporal cache update
         // cache_out[k] is frame T - 2 + k of (cache_in or zeros) ++ x_chunk: the input frame that
-        // the last frame group stages as j = G + k.  This warp follows the stage ring and has the
-        // TMA unit store the interior of those stages (the segment's output rows; the strip's
-        // 126 pixels, staged from row 8 on, a swizzle-atom boundary) to cache_out, so the history
-        // is written from shared memory without a second read of x.
+        // the last frame group stages as j = G + k.  This warp follows the stage ring and writes
+        // the segment's output rows of those stages to cache_out from shared memory, so x is not
+        // read a second time: the TMA unit stores staged rows 8 .. 127 (a store must start on a
+        // swizzle atom), and the warp's lanes copy rows 1 .. 7 themselves, undoing the 64-byte
+        // swizzle (16-byte chunk c of staged row r sits at chunk c ^ ((r >> 1) & 3)).
+        __nv_bfloat16* hist = reinterpret_cast<__nv_bfloat16*>(L.cache_out);
         int s = 0, ph = 0;
         bool ok = true;
         for (long long u = ubeg; ok && u < uend;) {
@@ -303,14 +312,29 @@ __global__ void __launch_bounds__(kThreads, 1) head_bf16_kernel(const __grid_con
                         ok = false;
                         break;
                     }
-                    if (lane == 0 && last_group && j >= g.G && hin >= g.h0 && hin < g.h1) {
+                    if (last_group && j >= g.G && hin >= g.h0 && hin < g.h1) {
                         const uint8_t* stage = smX + (size_t)s * L.x_stage_bytes;
-                        fence_proxy_async_smem();
-                        for (int cb = 0; cb < ncb; ++cb)
-                            tma_store_4d(&L.map_cache_out, stage + (size_t)(cb * kHeadBox + kHeadLead) * ROWB,
-                                         cb * kHeadCB, g.w0, hin, j - g.G);
-                        bulk_commit_group();
-                        bulk_wait_group_read<0>();  // the stage may be refilled once the store has read it
+                        constexpr int NLEAD = kHeadStoreRow - kHeadLead;  // positions w0 .. w0 + 6
+                        for (int i = lane; i < NLEAD * ncb * 4; i += 32) {
+                            const int c = i & 3, rest = i >> 2;
+                            const int r = kHeadLead + rest % NLEAD, cb = rest / NLEAD;
+                            const int w = g.w0 + r - kHeadLead;
+                            if (w < L.W) {
+                                const uint4 v = *reinterpret_cast<const uint4*>(
+                                    stage + (size_t)(cb * kHeadBox + r) * ROWB + ((c ^ ((r >> 1) & 3)) << 4));
+                                *reinterpret_cast<uint4*>(
+                                    hist + (((size_t)(j - g.G) * L.H + hin) * L.W + w) * L.Cin + cb * kHeadCB + c * 8) = v;
+                            }
+                        }
+                        // (frames narrower than 8 pixels have nothing in the TMA store's box)
+                        if (lane == 0 && g.w0 + kHeadStoreRow - kHeadLead < L.W) {
+                            fence_proxy_async_smem();
+                            for (int cb = 0; cb < ncb; ++cb)
+                                tma_store_4d(&L.map_cache_out, stage + (size_t)(cb * kHeadBox + kHeadStoreRow) * ROWB,
+                                             cb * kHeadCB, g.w0 + kHeadStoreRow - kHeadLead, hin, j - g.G);
+                            bulk_commit_group();
+                            bulk_wait_group_read<0>();  // the stage may be refilled once the store has read it
+                        }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&x_empty[s]);

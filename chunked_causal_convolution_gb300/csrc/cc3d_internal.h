@@ -103,10 +103,10 @@ cudaError_t tc2s_launch(int CB, const TcLaunch& L, cudaStream_t stream);
 
 // Narrow-output kernel (Cout <= 5): the nine spatial taps stacked into N, rows streamed once.
 struct HeadLaunch {
-    CUtensorMap map_x;          // x_chunk   [T][H][W][Cin]  box (32, 136, 1, 1)
+    CUtensorMap map_x;          // x_chunk   [T][H][W][Cin]  box (32, 128, 1, 1)
     CUtensorMap map_cache;      // cache_in  [2][H][W][Cin]  same box (unused if no cache)
     CUtensorMap map_w;          // w viewed as (Cin, Cout, 27 taps)  box (32, Cout, 9)
-    CUtensorMap map_cache_out;  // cache_out [2][H][W][Cin]  box (32, 126, 1, 1), stored from shared memory
+    CUtensorMap map_cache_out;  // cache_out [2][H][W][Cin]  box (32, 120, 1, 1), stored from shared memory
     int T, H, W, Cin, Cout;
     int gmax;               // output frames per pass over the rows
     int ncolblk;            // column strips of 126 output pixels

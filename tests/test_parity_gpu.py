@@ -59,6 +59,8 @@ SMALL = [
     ("bf16_cb16_one_sm_wide_n", "bf16", 16, 192, 3, 5, 40, [2, 1], True, False),
     # a 4-channel narrow head
     ("bf16_head_cout4", "bf16", 96, 4, 4, 5, 140, [3, 1], True, True),
+    # a head on frames narrower than the 8 pixels the lanes copy of the history
+    ("bf16_head_narrow_frame", "bf16", 32, 3, 3, 4, 5, [2, 1], True, False),
 ]
 
 
@@ -72,7 +74,7 @@ SMALL_KERNEL = {
     "bf16_two_flat_blocks": "tc_bf16", "bf16_c192_like": "tc_bf16", "bf16_one_pixel": "tc_bf16",
     "bf16_c96_wide_flat_window": "tc_bf16", "bf16_c256_narrow_column_blocks": "tc_bf16",
     "bf16_cb16_pairs_row_aligned": "tc_bf16_pair", "bf16_cb16_one_sm_wide_n": "tc_bf16",
-    "bf16_head_cout4": "tc_bf16_head",
+    "bf16_head_cout4": "tc_bf16_head", "bf16_head_narrow_frame": "tc_bf16_head",
 }
 
 

@@ -23,10 +23,23 @@ kt - 1 frames first waits for its own history, then sends; rank 0 never waits, s
     layers = [ChunkedLayer(plan1, w1, b1), ChunkedLayer(plan2, w2, b2)]
     split = TimeSplit(layers)                 # inside an initialised process group
     y_local = split.forward(x_local)          # this rank's frames of one wave
+
+The height split ("SGLang-Diffusion advanced optimizations", section 3 "Parallel VAE": every rank
+takes a band of rows, exchanges halo rows with its neighbours, and the bands are gathered at the
+end): every rank owns a contiguous band of rows of every frame and runs each layer on its band
+extended by the (kh - 1) / 2 rows above and below that its neighbours send it.  The outputs of the
+band's own rows equal the whole frame's (the rows outside the frame are the conv's zero padding,
+the rows from the neighbours are the real ones); the extended rows' outputs are dropped.  Each
+rank keeps its layers' temporal histories itself (of its extended band, halo rows included).
+
+    split = HeightSplit([ChunkedLayer(plan_band1, w1, b1), ...])   # plans of the extended band
+    y_band = split.forward(x_band)            # one chunk of this rank's rows
+    y = split.gather(y_band, H)               # every rank's bands, whole frames
 """
 from __future__ import annotations
 
-__all__ = ["frame_ranges", "end_history", "exchange", "TimeSplit", "ChunkedLayer"]
+__all__ = ["frame_ranges", "end_history", "exchange", "TimeSplit", "ChunkedLayer", "row_ranges",
+           "band_extent", "HeightSplit"]
 
 
 def frame_ranges(T: int, world: int):
@@ -159,6 +172,94 @@ class TimeSplit:
         return x
 
 
+def row_ranges(H: int, world: int):
+    """Contiguous row bands [(start, stop)] of H-row frames over `world` ranks (as frame_ranges)."""
+    return frame_ranges(H, world)
+
+
+def band_extent(H: int, world: int, rank: int, halo: int):
+    """(first, stop) rows of rank's band extended by `halo` rows on each side that lies inside
+    the frame: the rows a layer with a (2 * halo + 1)-row spatial kernel reads for the band."""
+    a, b = row_ranges(H, world)[rank]
+    return max(0, a - halo), min(H, b + halo)
+
+
+class HeightSplit:
+    """A stack of layers run on this rank's band of rows, with the halo-row exchange before every
+    layer.  Each layer is a callable (x_extended, history) -> y_extended with attributes P (= kt - 1)
+    and halo (= (kh - 1) / 2); it is run on the band extended by up to `halo` rows above and below
+    (the neighbours' rows; none beyond the frame's edge) and must be built for that height (see
+    band_extent).  The layer's temporal history (of the extended band) stays on the rank: the
+    history a layer returns through its attribute `last_history` after a call is passed back to it
+    on the next chunk (None: zero history, the first chunk of a video)."""
+
+    def __init__(self, layers, group=None):
+        self.layers = list(layers)
+        self.group = group
+        self.histories = [None] * len(self.layers)
+
+    def reset(self):
+        self.histories = [None] * len(self.layers)
+
+    def _extend(self, x, halo, rank, world):
+        """x [T][h][W][C] (this rank's band) -> the band with `halo` neighbour rows on each side
+        that has a neighbour, and the number of rows added on top."""
+        import torch
+        import torch.distributed as dist
+        if halo == 0 or world == 1:
+            return x, 0
+        if int(x.shape[1]) < halo:
+            raise ValueError("every band needs at least the halo's rows")
+        up, down = _global_rank(self.group, rank - 1), _global_rank(self.group, rank + 1)
+        reqs, keep = [], []
+        top = bottom = None
+        shape = (x.shape[0], halo) + tuple(x.shape[2:])
+        if rank > 0:
+            top = torch.empty(shape, dtype=x.dtype, device=x.device)
+            reqs.append(dist.irecv(top, src=up, group=self.group, tag=1))
+            first = x[:, :halo].contiguous()
+            keep.append(first)
+            reqs.append(dist.isend(first, dst=up, group=self.group, tag=2))
+        if rank < world - 1:
+            bottom = torch.empty(shape, dtype=x.dtype, device=x.device)
+            reqs.append(dist.irecv(bottom, src=down, group=self.group, tag=2))
+            last = x[:, int(x.shape[1]) - halo:].contiguous()
+            keep.append(last)
+            reqs.append(dist.isend(last, dst=down, group=self.group, tag=1))
+        for r in reqs:
+            r.wait()
+        parts = [p for p in (top, x, bottom) if p is not None]
+        return torch.cat(parts, 1), (halo if top is not None else 0)
+
+    def forward(self, x_band):
+        rank, world = _group_info(self.group)
+        x = x_band
+        for i, layer in enumerate(self.layers):
+            halo = int(getattr(layer, "halo", 0))
+            xe, top = self._extend(x, halo, rank, world)
+            y = layer(xe, self.histories[i] if int(layer.P) > 0 else None)
+            if int(layer.P) > 0:
+                self.histories[i] = layer.last_history
+            x = y[:, top:top + int(x.shape[1])]
+        return x
+
+    def gather(self, y_band, H: int):
+        """Every rank's band of the output, whole frames [T][H][W][C], on every rank."""
+        import torch
+        import torch.distributed as dist
+        rank, world = _group_info(self.group)
+        if world == 1:
+            return y_band
+        ranges = row_ranges(H, world)
+        hmax = max(b - a for a, b in ranges)
+        pad = torch.zeros((y_band.shape[0], hmax) + tuple(y_band.shape[2:]), dtype=y_band.dtype,
+                          device=y_band.device)
+        pad[:, :int(y_band.shape[1])] = y_band
+        bufs = [torch.empty_like(pad) for _ in range(world)]
+        dist.all_gather(bufs, pad, group=self.group)
+        return torch.cat([bufs[r][:, :b - a] for r, (a, b) in enumerate(ranges)], 1)
+
+
 class ChunkedLayer:
     """One layer of the library run over a rank's frames: the chunk loop with the two ping-pong
     history buffers, the first chunk reading the history the exchange delivered.  plan is a
@@ -169,7 +270,9 @@ class ChunkedLayer:
             raise ValueError("chunk >= 1")
         self.plan, self.w, self.b, self.chunk, self.stream = plan, w, b, int(chunk), stream
         self.P = plan.kt - 1
+        self.halo = (plan.kh - 1) // 2
         self._caches = None
+        self.last_history = None  # the history the last call left (the input frames after it need)
 
     def __call__(self, x, history, residual=None):
         import torch
@@ -177,13 +280,18 @@ class ChunkedLayer:
         y = torch.empty((T, self.plan.Ho, self.plan.Wo, self.plan.Cout), dtype=self.plan.torch_dtype(),
                         device=x.device)
         if self.P > 0 and self._caches is None:
-            self._caches = [self.plan.new_cache(x.device), self.plan.new_cache(x.device)]
+            # three buffers: the two the chunks alternate between, and a third so that neither of
+            # them is the history passed in (which may be the one the previous call left)
+            self._caches = [self.plan.new_cache(x.device) for _ in range(3)]
+        if self.P > 0:
+            free = [c for c in self._caches if history is None or c.data_ptr() != history.data_ptr()][:2]
         s, k = 0, 0
         while s < T:
             c = min(self.chunk, T - s)
             if self.P > 0:
-                cin = history if k == 0 else self._caches[(k - 1) % 2]
-                cout = self._caches[k % 2]
+                cin = history if k == 0 else free[(k - 1) % 2]
+                cout = free[k % 2]
+                self.last_history = cout
             else:
                 cin = cout = None
             self.plan.forward_chunk(x[s:s + c], self.w, self.b, None if residual is None else residual[s:s + c],

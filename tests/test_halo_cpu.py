@@ -163,3 +163,85 @@ def test_single_layer_exchange_over_gloo_ranks():
         out = m.dict()
         mp.spawn(_exchange_main, args=(3, _free_port(), out), nprocs=3, join=True)
         assert dict(out) == {0: True, 1: True, 2: True}
+
+
+# ---------------------------------------------------------------- height split
+
+HS_LAYERS = [(3, 4, 3, 3), (4, 2, 2, 3), (2, 3, 1, 1)]  # (Cin, Cout, kt, kh = kw)
+
+
+def _band_video(T, H, W):
+    sys.path.insert(0, ROOT)
+    import synth
+    e = synth.dense_index
+    x = synth.bf16_bits_to_f64(synth.raw(41, synth.TID_X, synth.Dist.normal(1.0), e((T, H, W, HS_LAYERS[0][0])), "bf16"))
+    ws, bs = [], []
+    for j, (ci, co, kt, ks) in enumerate(HS_LAYERS):
+        ws.append(synth.bf16_bits_to_f64(synth.raw(50 + j, synth.TID_W, synth.Dist.normal(synth.fan_in_sigma(ci, kt, ks, ks)),
+                                                   e((co, kt, ks, ks, ci)), "bf16")))
+        bs.append(synth.bf16_bits_to_f64(synth.raw(50 + j, synth.TID_B, synth.Dist.uniform(-0.1, 0.1), e((co,)), "bf16")))
+    return x, ws, bs
+
+
+class OracleBandLayer:
+    """A layer on an extended band, computed by the oracle's chunk form; keeps its history."""
+
+    def __init__(self, w, b):
+        self.w, self.b = w, b
+        self.P = w.shape[1] - 1
+        self.halo = (w.shape[2] - 1) // 2
+        self.last_history = None
+
+    def __call__(self, x, history):
+        import oracle
+        y, cache = oracle.conv_chunk(x.numpy(), self.w, self.b, None,
+                                     None if history is None else history.numpy(), nthreads=1)
+        self.last_history = torch.from_numpy(cache)
+        return torch.from_numpy(y)
+
+
+def _height_main(rank, world, port, H, chunks, out):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import oracle
+    from chunked_causal_convolution_gb300 import halo
+    dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank, world_size=world)
+    try:
+        T, W = sum(chunks), 5
+        x, ws, bs = _band_video(T, H, W)
+        ref = x
+        for w, b in zip(ws, bs):
+            ref = oracle.conv_whole(ref, w, b, nthreads=1)
+        a, b_ = halo.row_ranges(H, world)[rank]
+        split = halo.HeightSplit([OracleBandLayer(w, b) for w, b in zip(ws, bs)])
+        errs, gathered_ok, s = [], True, 0
+        for c in chunks:
+            y = split.forward(torch.from_numpy(x[s:s + c, a:b_]))
+            errs.append(float(np.abs(y.numpy() - ref[s:s + c, a:b_]).max()))
+            full = split.gather(y, H)
+            gathered_ok &= bool(np.array_equal(full.numpy(), ref[s:s + c]))
+            s += c
+        out[rank] = (max(errs), gathered_ok)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,H,chunks", [(2, 7, [4, 2]), (3, 8, [1, 3, 2])])
+def test_height_split_over_gloo_ranks_equals_the_whole_frame(world, H, chunks):
+    sys.path.insert(0, ROOT)
+    import oracle
+    oracle.build()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_height_main, args=(world, _free_port(), H, chunks, out), nprocs=world, join=True)
+        res = dict(out)
+    assert sorted(res) == list(range(world))
+    for r, (err, gathered_ok) in res.items():
+        assert err == 0.0, (r, err)
+        assert gathered_ok, r
+
+
+def test_band_extent():
+    from chunked_causal_convolution_gb300 import halo
+    assert [halo.band_extent(8, 3, r, 1) for r in range(3)] == [(0, 4), (2, 7), (5, 8)]
+    assert halo.band_extent(8, 1, 0, 1) == (0, 8)

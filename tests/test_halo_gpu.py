@@ -55,3 +55,40 @@ def test_waves_through_the_time_split_equal_the_chunk_loop():
         inp = got
     for plan in plans:
         plan.close()
+
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_bands_of_the_height_split_equal_the_whole_frame(world):
+    """Every rank's layer run on its band extended by the halo rows (as halo.HeightSplit arranges
+    it, with the rank's own history carried from chunk to chunk) gives, for the band's own rows,
+    exactly the bits of the whole-frame chunk loop: every output's accumulation order does not
+    depend on the frame's height.  The ranks run one after another on one GPU, layer by layer (the
+    layer's input rows for every band come from the previous layer's output, which is what the
+    exchange delivers); the exchange itself is tested over gloo ranks."""
+    T, H, W, chunks = 6, 11, 128, [4, 2]
+    spec = [(96, 96, 3), (96, 32, 2), (32, 3, 3)]  # SM pairs, MemoryBlock-like, narrow head
+    x = to_device(small_inputs(96, 96, T, H, W, "bf16", 640, bias=False)["x"], "bf16")
+    cur = x
+    for j, (ci, co, kt) in enumerate(spec):
+        p = small_inputs(ci, co, 1, 1, 1, "bf16", 650 + j, bias=True, k=(kt, 3, 3))
+        w, b = to_device(p["w"], "bf16"), to_device(p["b"], "bf16")
+        whole = cc3d.CausalConv3dPlan(ci, co, H, W, kt, 3, 3)
+        ref, _ = run_chunks(whole, cur, w, b, None, chunks)
+        bands = []
+        for r in range(world):
+            a, b_ = halo.row_ranges(H, world)[r]
+            e0, e1 = halo.band_extent(H, world, r, 1)
+            plan = cc3d.CausalConv3dPlan(ci, co, e1 - e0, W, kt, 3, 3)
+            layer = halo.ChunkedLayer(plan, w, b)
+            hist, outs, s0 = None, [], 0
+            for c in chunks:
+                outs.append(layer(cur[s0:s0 + c, e0:e1].contiguous(), hist))
+                hist = layer.last_history
+                s0 += c
+            assert plan.status() == 0
+            bands.append(torch.cat(outs)[:, a - e0:b_ - e0])
+            plan.close()
+        assert torch.equal(torch.cat(bands, 1), ref), (world, j)
+        whole.close()
+        cur = ref

@@ -16,6 +16,8 @@
 //     accumulator is complete after its last tap (the input frame t_out itself), so the epilogue
 //     drains frame 0 while the MMAs still run on later frames, and the next unit's frame 0 only
 //     needs frame 0's columns back;
+//   * two MMA warps take the output frames of a unit by parity (each accumulator has one writer),
+//     so that one warp's issue stalls are covered by the other's MMAs;
 //   * the new history (the last P input frames) is stored from the staged blocks by the copy
 //     engine.
 //
@@ -73,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
     float* s_bias = reinterpret_cast<float*>(smX + (size_t)L.nstages * L.x_stage_bytes);
 
     __shared__ uint64_t x_full[kSMaxStages], x_empty[kSMaxStages], w_full, acc_full[kSMaxFrames],
-        acc_empty[kSMaxFrames], mma_drain;
+        acc_empty[kSMaxFrames], mma_drain[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
 
@@ -88,11 +90,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        // a stage is released by the MMA warp and, when there is a history to write, the copy warp
-        for (int s = 0; s < nst; ++s) { mbar_init(&x_full[s], 1); mbar_init(&x_empty[s], P > 0 ? 2 : 1); }
+        // a stage is released by both MMA warps and, when there is a history to write, the copy warp
+        for (int s = 0; s < nst; ++s) { mbar_init(&x_full[s], 1); mbar_init(&x_empty[s], P > 0 ? 3 : 2); }
         mbar_init(&w_full, 1);
         for (int f = 0; f < L.gmax; ++f) { mbar_init(&acc_full[f], 1); mbar_init(&acc_empty[f], 4); }
-        mbar_init(&mma_drain, 1);
+        mbar_init(&mma_drain[0], 1);
+        mbar_init(&mma_drain[1], 1);
         fence_mbar_init();
     }
     if (warp >= 4) {
@@ -155,9 +158,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
                     atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
             if (!bounded_wait(&w_full, 0, budget, nullptr)) atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA warp
-        // lane 0 polls the barriers and issues every MMA and commit
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA warps
+        // warp 1 owns the unit's even output frames, warp 2 the odd ones; lane 0 of each polls the
+        // barriers and issues its MMAs and commits
+        const int k = warp - 1;
         const bool lead = lane == 0;
         const uint32_t idesc = make_idesc_bf16_f32(128, Cout);
         const uint64_t x_desc0 = make_sdesc(smem_u32(smX), 16, SBO, LAYOUT_SW64, 0);
@@ -180,9 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
                 }
                 tc_fence_after();
                 const uint64_t xs = desc_add(x_desc0, s * x_inc);
+                bool any = false;
                 for (int dt = 0; dt < L.kt; ++dt) {
                     const int tout = j - dt;  // input frame t0 - P + j is tap dt of output frame t0 + tout
-                    if (tout < 0 || tout >= g.G) continue;
+                    if (tout < 0 || tout >= g.G || (tout & 1) != k) continue;
+                    any = true;
                     if (dt == 0) {
                         // first tap of this frame: its slot must have been drained by the epilogue
                         const uint32_t par = ((slot_phase >> tout) & 1u) ^ 1u;
@@ -211,14 +218,18 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
                     }
                 }
                 if (!ok) break;
-                if (lead) umma_commit(&x_empty[s]);
+                // a warp that read nothing from this stage releases it at once
+                if (lead) {
+                    if (any) umma_commit(&x_empty[s]);
+                    else mbar_arrive(&x_empty[s]);
+                }
                 __syncwarp();
                 if (++s == nst) { s = 0; ph ^= 1; }
             }
         }
-        if (lead) umma_commit(&mma_drain);
+        if (lead) umma_commit(&mma_drain[k]);
         __syncwarp();
-        if (!warp_bounded_wait(&mma_drain, 0, budget, nullptr) && lane == 0) atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
+        if (!warp_bounded_wait(&mma_drain[k], 0, budget, nullptr) && lane == 0) atomicOr(L.status, STATUS_TIMEOUT_DRAIN);
     } else if (warp == 3) {
         // ------------------------------------------------------------ temporal cache update
         // cache_out[k] is input frame T - P + k, which the last frame group stages as j = G + k:

@@ -17,7 +17,8 @@
 //     drains frame 0 while the MMAs still run on later frames, and the next unit's frame 0 only
 //     needs frame 0's columns back;
 //   * two MMA warps take the output frames of a unit by parity (each accumulator has one writer),
-//     so that one warp's issue stalls are covered by the other's MMAs;
+//     so that one warp's issue stalls are covered by the other's MMAs, and two sets of four
+//     epilogue warps drain them by the same parity;
 //   * the new history (the last P input frames) is stored from the staged blocks by the copy
 //     engine.
 //
@@ -39,6 +40,9 @@ constexpr int kSCB = 32;          // channels per staged block: 64-byte rows, 64
 constexpr int kSPos = 128;        // positions per unit (the MMA's M)
 constexpr int kSMaxStages = 8;    // input-frame stages
 constexpr int kSMaxFrames = 8;    // output frames per unit (tensor-memory slots)
+// warps: 0 loader, 1-2 MMA, 3 history stores, 4-7 and 8-11 the two epilogue sets (warp w reads
+// tensor-memory lanes 32 * (w % 4) ..)
+constexpr int kSThreads = 384;
 
 struct SUnit {
     int t0, G;   // output frames [t0, t0 + G)
@@ -62,7 +66,7 @@ __device__ __forceinline__ void s_fail(const StreamLaunch& L, unsigned bit, vola
     atomicOr(L.status, bit);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_constant__ StreamLaunch L)
+__global__ void __launch_bounds__(kSThreads, 1) stream_bf16_kernel(const __grid_constant__ StreamLaunch L)
 {
     constexpr uint32_t ROWB = kSCB * 2;
     constexpr uint32_t SBO = 8 * ROWB;
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
     }
     if (warp >= 4) {
         const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(L.bias);
-        for (int i = threadIdx.x - 128; i < Cout; i += 128)
+        for (int i = threadIdx.x - 128; i < Cout; i += kSThreads - 128)
             s_bias[i] = b != nullptr ? __bfloat162float(b[i]) : 0.0f;
     }
     if (warp == 2) {
@@ -263,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
-        const int q = warp - 4;  // tensor-memory lanes 32q .. 32q+31 = positions p0 + 32q + lane
+        const int q = (warp - 4) % 4;  // tensor-memory lanes 32q .. 32q+31 = positions p0 + 32q + lane
+        const int set = (warp - 4) / 4;  // this set drains the output frames of its parity
         const __nv_bfloat16* res = reinterpret_cast<const __nv_bfloat16*>(L.res);
         __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(L.y);
         const bool wide = (Cout % 16) == 0;
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_bf16_kernel(const __grid_c
             const SUnit g = s_unit(L, u);
             const long long p = (long long)g.p0 + q * 32 + lane;
             const bool pvalid = p < HW;
-            for (int tout = 0; tout < g.G; ++tout) {
+            for (int tout = set; tout < g.G; tout += 2) {
                 int ready = 0;
                 if (lane == 0) {
                     ready = bounded_wait(&acc_full[tout], (slot_phase >> tout) & 1u, budget, &abort_flag,
@@ -343,7 +348,7 @@ cudaError_t stream_launch(const StreamLaunch& L, cudaStream_t stream)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem_bytes);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<StreamLaunch*>(&L)};
-    return cudaLaunchKernel(kern, dim3(L.grid), dim3(kThreads), args, L.smem_bytes, stream);
+    return cudaLaunchKernel(kern, dim3(L.grid), dim3(kSThreads), args, L.smem_bytes, stream);
 }
 
 }  // namespace cc3d

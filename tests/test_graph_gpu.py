@@ -151,3 +151,57 @@ def test_graph_replay_of_sm_pair_chunks_with_the_side_stream_copy(Tc):
                             to_f64(a["r"], "bf16"))
     assert np.abs(from_device(y_eager) - ref).max() <= tolerance("bf16", ref)
     plan.close()
+
+
+def test_graph_replay_of_a_frame_batched_layer_group_is_bit_identical():
+    """A layer group (frame batches of one frame through a 3x3x3 conv and the 3-channel head) is
+    captured into one CUDA graph per history parity over fixed buffers and a fixed workspace; the
+    video streamed through the graphs equals the eager group calls bit for bit, outputs and both
+    histories."""
+    T, H, W, C, a, h = _layers()
+    Tc = 4
+    x = to_device(a["x"], "bf16")
+    ws = [to_device(a["w"], "bf16"), to_device(h["w"], "bf16")]
+    bs = [to_device(a["b"], "bf16"), to_device(h["b"], "bf16")]
+    plans = [cc3d.CausalConv3dPlan(C, C, H, W), cc3d.CausalConv3dPlan(C, 3, H, W)]
+    group = cc3d.LayerGroup(plans, 1)
+    work = group.new_workspace(Tc)
+
+    eager_c = [[p.new_cache(), p.new_cache()] for p in plans]
+    ys = []
+    for k in range(T // Tc):
+        ys.append(group.forward_chunk(x[k * Tc:(k + 1) * Tc], ws, bs, [c[k % 2] for c in eager_c] if k else None,
+                                      [c[(k + 1) % 2] for c in eager_c], workspace=work))
+    y_eager = torch.cat(ys)
+    torch.cuda.synchronize()
+    assert all(p.status() == 0 for p in plans)
+
+    xs = torch.empty((Tc, H, W, C), dtype=torch.bfloat16, device="cuda")
+    yb = torch.empty((Tc, H, W, 3), dtype=torch.bfloat16, device="cuda")
+    gc = [[p.new_cache(), p.new_cache()] for p in plans]
+    s = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(s):
+        # warm-up outside capture (the plans create their side streams on first use)
+        group.forward_chunk(xs, ws, bs, None, [c[1] for c in gc], yb, workspace=work, stream=s)
+    s.synchronize()
+    for par in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            group.forward_chunk(xs, ws, bs, [c[par] for c in gc], [c[1 - par] for c in gc], yb, workspace=work,
+                                stream=s)
+        graphs.append(g)
+    for p, c in zip(plans, gc):
+        p.reset(c[0])  # the video's zero history, read by the first replay
+    torch.cuda.synchronize()
+    out = []
+    for k in range(T // Tc):
+        xs.copy_(x[k * Tc:(k + 1) * Tc])
+        graphs[k % 2].replay()  # chunk k reads histories [k % 2] (zeros for k = 0), writes [(k + 1) % 2]
+        out.append(yb.clone())
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(out), y_eager)
+    for p_c, e_c in zip(gc, eager_c):
+        assert torch.equal(p_c[(T // Tc) % 2], e_c[(T // Tc) % 2])
+    assert all(p.status() == 0 for p in plans)
+    group.close()

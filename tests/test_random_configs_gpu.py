@@ -115,3 +115,26 @@ def test_random_layer_matches_the_oracle_and_every_chunking(case):
     err = np.abs(from_device(ys[0]) - ref).max()
     assert err <= tolerance(c["dtype"], ref), (plan.kernel, c, err)
     plan.close()
+
+
+# Medium shapes with more tiles than the SMs hold at once: several tiles per block or pair, the
+# one-SM kernel's split last wave, the streaming kernel's runs of units, many head strips.
+MEDIUM = [
+    dict(kind="conv", dtype="bf16", Cin=192, Cout=192, T=3, H=90, W=160, kt=3, k=3, bias=True, residual=True,
+         chunks=[[3], [1, 2]]),                       # one SM, 171 tiles: the last 19 split
+    dict(kind="two_frame", dtype="bf16", Cin=96, Cout=96, T=4, H=128, W=256, kt=3, k=3, bias=True,
+         residual=True, chunks=[[4], [2, 2]]),        # two-frame pairs, two pair tiles per pair
+    dict(kind="conv", dtype="bf16", Cin=128, Cout=128, T=4, H=60, W=200, kt=2, k=3, bias=False, residual=True,
+         chunks=[[4], [2, 2]]),                       # flat pairs, 96 pair tiles on 76 pairs
+    dict(kind="conv1x1", dtype="bf16", Cin=64, Cout=128, T=5, H=80, W=200, kt=3, k=1, bias=True,
+         residual=False, chunks=[[5], [4, 1]]),       # streaming kernel, 250 units
+    dict(kind="head", dtype="bf16", Cin=96, Cout=3, T=4, H=64, W=512, kt=3, k=3, bias=True, residual=False,
+         chunks=[[4], [1, 3]]),                       # narrow head, many strips
+    dict(kind="up2", dtype="bf16", Cin=64, Cout=64, T=3, H=48, W=80, kt=3, k=3, bias=True, residual=False,
+         chunks=[[3], [2, 1]]),                       # fused upsample, 96 x 160 outputs
+]
+
+
+@pytest.mark.parametrize("case", MEDIUM, ids=[_id(c) for c in MEDIUM])
+def test_medium_layer_matches_the_oracle_and_every_chunking(case):
+    test_random_layer_matches_the_oracle_and_every_chunking(case)

@@ -116,3 +116,60 @@ def test_group_empty_chunk_moves_every_history():
             assert torch.equal(a, b)
     group.close()
 
+
+
+def _random_stacks(n=16, seed=7021):
+    rng = np.random.RandomState(seed)
+    out = []
+    for _ in range(n):
+        nl = int(rng.randint(2, 5))
+        c = int(rng.choice([16, 32, 48, 64]))
+        stack, used_up2 = [], False
+        for _ in range(nl):
+            co = int(rng.choice([16, 32, 48, 64]))
+            up2 = (not used_up2) and rng.rand() < 0.2
+            used_up2 |= up2
+            kt = int(rng.randint(1, 4))
+            k = 3 if up2 else int(rng.choice([1, 3]))
+            stack.append((c, co, (kt, k, k), bool(up2)))
+            c = co
+        T = int(rng.randint(2, 8))
+        cuts = sorted(rng.choice(np.arange(1, T), size=rng.randint(0, min(2, T - 1) + 1), replace=False))
+        bounds = [0] + [int(x) for x in cuts] + [T]
+        chunks = [b - a for a, b in zip(bounds, bounds[1:])]
+        out.append(dict(stack=stack, H=int(rng.randint(2, 7)), W=int(rng.randint(8, 41)), T=T, chunks=chunks,
+                        frame_batch=int(rng.choice([0, 1, 2, 3, 5]))))
+    return out
+
+
+RANDOM_STACKS = _random_stacks()
+
+
+@pytest.mark.parametrize("case", RANDOM_STACKS, ids=["stack%d_fb%d" % (i, c["frame_batch"])
+                                                     for i, c in enumerate(RANDOM_STACKS)])
+def test_random_group_equals_the_layer_by_layer_chunk_loop(case):
+    """Random stacks of 2-4 layers (any kt, 1x1 or 3x3, at most one fused upsample), random
+    chunkings and frame batches: the group's output and every layer's history after each chunk
+    equal those of each layer's own chunk loop, bit for bit."""
+    stack, H, W, T, chunks = case["stack"], case["H"], case["W"], case["T"], case["chunks"]
+    plans, params = _make(stack, H, W, 40 + len(stack) + H + W)
+    raw = small_inputs(stack[0][0], stack[0][1], T, H, W, "bf16", 60 + T + W, bias=False)
+    x = to_device(raw["x"], "bf16")
+    outs_ref, hists_ref = _layer_by_layer(plans, params, x, chunks)
+    group = cc3d.LayerGroup(plans, case["frame_batch"])
+    ws = group.new_workspace(max(chunks))
+    caches = [[p.new_cache(), p.new_cache()] if p.kt > 1 else [None, None] for p in plans]
+    ys, s = [], 0
+    for k, c in enumerate(chunks):
+        ys.append(group.forward_chunk(x[s:s + c], [q[0] for q in params], [q[1] for q in params],
+                                      [c_[k % 2] if k else None for c_ in caches],
+                                      [c_[(k + 1) % 2] for c_ in caches], workspace=ws))
+        for j, c_ in enumerate(caches):
+            if c_[0] is not None:
+                assert torch.equal(c_[(k + 1) % 2], hists_ref[k][j]), (case, k, j)
+        s += c
+    assert all(p.status() == 0 for p in plans)
+    assert torch.equal(torch.cat(ys), outs_ref[-1]), case
+    group.close()
+    for p in plans:
+        p.close()

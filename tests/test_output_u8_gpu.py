@@ -84,3 +84,48 @@ def test_u8_head_equals_quantised_bf16_output(Cin, Cout, T, H, W, chunks, residu
     for alt in ([T], [1] * T):
         assert torch.equal(run_chunks_u8(plan, dev["x"], dev["w"], dev["b"], dev.get("r"), alt), yu8)
     plan.close()
+
+
+def _u8_cases(n=12, seed=818):
+    rng = np.random.RandomState(seed)
+    out = []
+    for _ in range(n):
+        T = int(rng.randint(2, 8))
+        cuts = sorted(rng.choice(np.arange(1, T), size=rng.randint(0, min(3, T - 1) + 1), replace=False))
+        b1 = [0] + [int(x) for x in cuts] + [T]
+        cuts2 = sorted(rng.choice(np.arange(1, T), size=rng.randint(0, min(3, T - 1) + 1), replace=False))
+        b2 = [0] + [int(x) for x in cuts2] + [T]
+        out.append(dict(Cin=int(rng.choice([32, 64, 96, 128])), Cout=int(rng.randint(1, 6)), T=T,
+                        H=int(rng.randint(1, 10)), W=int(rng.choice([int(rng.randint(1, 140)), 256, 300])),
+                        residual=bool(rng.randint(2)),
+                        chunks=[[b - a for a, b in zip(b1, b1[1:])], [b - a for a, b in zip(b2, b2[1:])]]))
+    return out
+
+
+U8_CASES = _u8_cases()
+
+
+@pytest.mark.parametrize("c", U8_CASES, ids=["%dto%d_T%d_%dx%d%s" % (c["Cin"], c["Cout"], c["T"], c["H"], c["W"],
+                                                                      "_r" if c["residual"] else "") for c in U8_CASES])
+def test_random_u8_heads_against_the_oracle_and_every_chunking(c):
+    """Random narrow heads and chunkings: the 8-bit pixels are bit-identical across chunkings,
+    equal to the plan's bf16 output quantised on the host, and inside the oracle's monotone
+    bounds."""
+    raw = small_inputs(c["Cin"], c["Cout"], c["T"], c["H"], c["W"], "bf16", 300 + c["T"] + c["W"], bias=True,
+                       residual=c["residual"])
+    dev = {k: to_device(v, "bf16") for k, v in raw.items()}
+    plan = cc3d.CausalConv3dPlan(c["Cin"], c["Cout"], c["H"], c["W"])
+    assert plan.kernel == "tc_bf16_head"
+    y, _ = run_chunks(plan, dev["x"], dev["w"], dev["b"], dev.get("r"), c["chunks"][0])
+    u1 = run_chunks_u8(plan, dev["x"], dev["w"], dev["b"], dev.get("r"), c["chunks"][0])
+    u2 = run_chunks_u8(plan, dev["x"], dev["w"], dev["b"], dev.get("r"), c["chunks"][1])
+    assert plan.status() == 0
+    assert torch.equal(u1, u2), c
+    got = u1.cpu().numpy()
+    assert np.array_equal(got, quant_u8(y)), c
+    ref = oracle.conv_whole(to_f64(raw["x"], "bf16"), to_f64(raw["w"], "bf16"), to_f64(raw["b"], "bf16"),
+                            to_f64(raw["r"], "bf16") if c["residual"] else None)
+    delta = ACC_BOUND * float(np.sqrt(np.mean(ref ** 2)))
+    lo, hi = oracle.quantize_u8(ref - delta), oracle.quantize_u8(ref + delta)
+    assert np.all((lo <= got) & (got <= hi)), (c, int(((lo > got) | (got > hi)).sum()))
+    plan.close()

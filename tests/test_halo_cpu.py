@@ -53,6 +53,8 @@ class OracleLayer:
 
     def __call__(self, x, history):
         import oracle
+        if int(x.shape[0]) == 0:  # an empty range: no output frames (the history passes through the split)
+            return torch.zeros((0,) + tuple(x.shape[1:3]) + (self.w.shape[0],), dtype=torch.float64)
         y, _ = oracle.conv_chunk(x.numpy(), self.w, self.b, None,
                                  None if history is None else history.numpy(), nthreads=1)
         return torch.from_numpy(y)
@@ -99,6 +101,8 @@ def _rank_main(rank, world, port, per_wave, waves, out):
     (2, [3, 3], 2),       # every range longer than the history
     (3, [1, 1, 2], 2),    # ranges shorter than the 2-frame history: the boundary chains through rank 1
     (2, [2, 1], 3),       # uneven ranges over three waves
+    (3, [2, 0, 2], 2),    # an empty range: rank 1 passes rank 0's boundary straight on
+    (4, [1, 0, 0, 2], 2), # two empty ranges in a row, and a 1-frame range before them
 ])
 def test_time_split_over_gloo_ranks_equals_the_whole_video(world, per_wave, waves):
     sys.path.insert(0, ROOT)

@@ -75,3 +75,27 @@ def test_workload_config_states_the_flop_count_and_the_l2_rule(name):
     assert "larger than L2" in cfg["l2"]
     # inputs larger than L2 is what lets the bench skip the flush
     assert wl.T * wl.H * wl.W * wl.Cin * 2 > 129e6
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores) prints exactly one JSON line
+    with the keys of the bench contract, on the headline workload, with no GPU."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "3", "--ref-rows", "2"], cwd=root, capture_output=True, text=True,
+                         timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] >= 3 and d["value"] > 0
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT and d["higher_is_better"] is True
+    assert d["config"]["workload"].startswith("c96_residual")
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0

@@ -80,12 +80,9 @@ def test_workload_config_states_the_flop_count_and_the_l2_rule(name):
 def test_reference_arm_prints_one_contract_line():
     """`bench.py --impl reference` (the fp64 oracle on the host cores) prints exactly one JSON line
     with the keys of the bench contract, on the headline workload, with no GPU."""
-    import json
     import subprocess
-    import sys
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "2",
-                          "--warmup", "3", "--ref-rows", "2"], cwd=root, capture_output=True, text=True,
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "3", "--ref-rows", "2"], cwd=ROOT, capture_output=True, text=True,
                          timeout=600)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.strip().startswith("{")]

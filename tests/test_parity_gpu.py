@@ -408,7 +408,8 @@ def test_non_default_stream():
 # one small plan of every tensor-core kernel family: (Cin, Cout, H, W, (kt, kh, kw), family)
 FAMILIES = [
     (32, 32, 6, 40, (3, 3, 3), "tc_bf16"),
-    (96, 96, 3, 256, (3, 3, 3), "tc_bf16_pair"),
+    (96, 96, 3, 256, (3, 3, 3), "tc_bf16_pair"),     # two-frame schedule
+    (64, 192, 4, 128, (3, 3, 3), "tc_bf16_pair"),    # one-frame schedule (192 output channels)
     (96, 3, 6, 130, (3, 3, 3), "tc_bf16_head"),
     (96, 96, 5, 70, (3, 1, 1), "tc_bf16_stream"),
     (48, 3, 5, 40, (3, 3, 3), "tc_bf16_narrow"),
@@ -423,7 +424,7 @@ def _family_case(Cin, Cout, H, W, k, family, T=4):
     return d, plan
 
 
-@pytest.mark.parametrize("case", FAMILIES, ids=[c[-1] for c in FAMILIES])
+@pytest.mark.parametrize("case", FAMILIES, ids=["%s_%d" % (c[-1], c[1]) for c in FAMILIES])
 def test_bounded_wait_times_out_and_the_context_survives(case):
     """The loader skips its first copy (test hook), a bounded wait runs out, the kernel records a
     timeout and every role leaves; the next call on the same context is correct."""
@@ -442,7 +443,7 @@ def test_bounded_wait_times_out_and_the_context_survives(case):
     plan.close()
 
 
-@pytest.mark.parametrize("case", FAMILIES, ids=[c[-1] for c in FAMILIES])
+@pytest.mark.parametrize("case", FAMILIES, ids=["%s_%d" % (c[-1], c[1]) for c in FAMILIES])
 def test_injected_host_encode_failure_launches_nothing(case):
     d, plan = _family_case(*case)
     plan.set_fault(2)
@@ -453,6 +454,24 @@ def test_injected_host_encode_failure_launches_nothing(case):
     assert e.value.code == 5
     torch.cuda.synchronize()
     assert torch.all(y.float() == 9.0)
+    plan.close()
+
+
+def test_bounded_wait_times_out_in_the_fused_upsample_and_the_context_survives():
+    raw = small_inputs(32, 64, 4, 4, 40, "bf16", 8, True, False)
+    d = {kk: to_device(v, "bf16") for kk, v in raw.items()}
+    plan = cc3d.Upsample2xConvPlan(32, 64, 4, 40, 3)
+    assert plan.kernel == "tc_bf16_up2"
+    y_ref, _ = run_chunks(plan, d["x"], d["w"], d["b"], None, [4])
+    plan.set_wait_budget_ns(50_000_000)
+    plan.set_fault(1)
+    y = torch.empty_like(y_ref)
+    plan.forward_chunk(d["x"], d["w"], d["b"], None, None, plan.new_cache(), y)
+    assert plan.status() == 7
+    plan.set_fault(0)
+    y2, _ = run_chunks(plan, d["x"], d["w"], d["b"], None, [4])
+    assert plan.status() == 0
+    assert torch.equal(y2, y_ref)
     plan.close()
 
 

@@ -132,6 +132,13 @@ MEDIUM = [
          chunks=[[4], [1, 3]]),                       # narrow head, many strips
     dict(kind="up2", dtype="bf16", Cin=64, Cout=64, T=3, H=48, W=80, kt=3, k=3, bias=True, residual=False,
          chunks=[[3], [2, 1]]),                       # fused upsample, 96 x 160 outputs
+    # the widest layers: 512 output channels in two 256-column blocks (N = 256 MMAs), 512 inputs
+    dict(kind="conv", dtype="bf16", Cin=64, Cout=512, T=4, H=3, W=40, kt=3, k=3, bias=True, residual=True,
+         chunks=[[4], [3, 1]]),
+    dict(kind="conv", dtype="bf16", Cin=512, Cout=64, T=4, H=4, W=40, kt=3, k=3, bias=True, residual=False,
+         chunks=[[4], [1, 3]]),
+    dict(kind="conv", dtype="bf16", Cin=512, Cout=512, T=3, H=2, W=24, kt=2, k=3, bias=False, residual=True,
+         chunks=[[3], [2, 1]]),
 ]
 
 

@@ -131,7 +131,11 @@ cc3d_status cc3d_plan_create_upsample2x(int Cin, int Cout, int H, int W, int kt,
  * zeros), and x_chunk, residual and y may be NULL.  A chunk of more than 2^33
  * positions (T_chunk * H * W) returns CC3D_ERR_UNSUPPORTED.
  * The result of every output element does not depend on how the video is
- * split into chunks (bit-identical across chunkings).
+ * split into chunks (bit-identical across chunkings).  (The chunk sees the
+ * previous chunk's last kt-1 input frames before its own: "SwiftVR Inference
+ * Optimization" (LightX2V blog), section "ReAE: Causal Halo Exchange"; chunked
+ * and whole-sequence results agree: "SGLang-Diffusion advanced optimizations",
+ * section 3 "Parallel VAE".)
  * Returns CC3D_OK once the work is enqueued; asynchronous failures surface in
  * cc3d_get_status.
  * Stream use: all work is ordered after what the caller enqueued earlier on
@@ -276,7 +280,11 @@ cc3d_status cc3d_group_forward_chunk_static(cc3d_group_t g, int T_chunk, const v
                                             void* const* cache_out, void* y, void* stream);
 
 /* Zero a cache buffer ([kt-1][H][W][Cin]) on the stream: the history of a new
- * video.  Stream-ordered, no allocation.  Same alignment rule as cache_out. */
+ * video.  Stream-ordered, no allocation.  Same alignment rule as cache_out.
+ * (A new stream restarts from a clean state without reallocating its buffers:
+ * "pixtreme-infer-cda-vsr" package page, section "Frame, state and stream
+ * requirements"; the first chunk's history is zeros: "SwiftVR Inference
+ * Optimization", section "ReAE: Causal Halo Exchange".) */
 cc3d_status cc3d_reset(cc3d_plan_t plan, void* cache, void* stream);
 
 /* Synchronise the stream, then report (and clear) the device status word and
